@@ -1,0 +1,134 @@
+/*
+ * flce.h - C ABI of the GB300 (sm_103a) fused linear cross-entropy library.
+ *
+ * Fused linear cross-entropy (FLCE) computes the loss of a final linear
+ * layer followed by cross-entropy without ever holding the [N, V] logits:
+ *
+ *   z[n, v]  = s * (x[n, :] . W[v, :] + b[v])
+ *   lse[n]   = log sum_v exp(z[n, v])
+ *   l[n]     = (1 - eps)(lse[n] - z[n, y_n]) + eps * lse[n]
+ *              - (eps / V) sum_v z[n, v] + lam * lse[n]^2      (0 if y_n == ignore_index)
+ *   loss     = l (none) | sum_n l[n] (sum) | sum_n l[n] / total (mean)
+ *
+ * and, in the backward pass, with g[n] the upstream gradient of token n's loss
+ * (dloss, dloss / total or dloss[n]; 0 for ignored tokens) and p = exp(z - lse):
+ *
+ *   dz[n, v] = g[n] * ((1 + 2 lam lse[n]) p[n, v] - eps / V - (1 - eps) [v == y_n])
+ *   dx = s dz W,   dW = s dz^T x,   db = s sum_n dz[n, :]
+ *
+ * Sources: the loss, label smoothing, logit_scale, ignore_index and the
+ * "mean over non-ignored tokens" rule follow the flash-linear-attention module
+ * fla/modules/fused_linear_cross_entropy.py (cross_entropy_kernel and
+ * fused_linear_cross_entropy_forward); the z-loss lam * lse^2 and the gradient
+ * (1 + 2 lam lse) softmax - eps/V - (1 - eps) delta follow Liger-Kernel PR #239
+ * "Support Z Loss in CE" (Details); reduction "none" and the "forward keeps
+ * only per-token softmax statistics, backward recomputes the logits one
+ * vocabulary block at a time" structure follow DeepSpeed PR #8792 ("What").
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *    except where a parameter says HOST. Tensors are dense and row-major.
+ *  - The caller owns every buffer, the workspace included. The library never
+ *    allocates or frees device memory and keeps no per-call state; calls are
+ *    stream-ordered on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *    and return without synchronising.
+ *  - Host-detectable errors (bad sizes, null or misaligned pointers, a small
+ *    workspace) return a status before anything is launched. Errors only the
+ *    device can see (an out-of-range target, a pipeline wait that timed out)
+ *    are OR-ed into the caller's device word `dev_err` (FLCE_DEVERR_* bits);
+ *    read it with flce_read_device_error after the stream has run. Outputs of
+ *    a call that raised a device error are unspecified. Kernels never trap.
+ */
+#ifndef FLCE_H_
+#define FLCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLCE_REDUCTION_NONE = 0, /* loss is [N] per-token losses */
+  FLCE_REDUCTION_SUM = 1,  /* loss is [1]: sum over tokens */
+  FLCE_REDUCTION_MEAN = 2  /* loss is [1]: sum / number of non-ignored tokens (0 if none) */
+} flce_reduction_t;
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARG = 1,       /* a size, option or required pointer is invalid */
+  FLCE_ERR_ALIGNMENT = 2,         /* a pointer or the hidden size breaks the 16-byte rules below */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 3,
+  FLCE_ERR_TARGET_OUT_OF_RANGE = 4, /* from flce_read_device_error */
+  FLCE_ERR_CUDA = 5,              /* a CUDA runtime call failed (launch, tensor-map encode) */
+  FLCE_ERR_TIMEOUT = 6,           /* from flce_read_device_error: a kernel wait gave up */
+  FLCE_ERR_UNSUPPORTED = 7        /* device is not sm_103 / sizes beyond the int32 tile grid */
+} flce_status_t;
+
+/* Device error word bits (see flce_read_device_error). */
+#define FLCE_DEVERR_TARGET 1
+#define FLCE_DEVERR_TIMEOUT 2
+
+typedef struct {
+  int64_t N;                /* tokens (rows of x); 0 is a valid no-op */
+  int64_t H;                /* hidden size; > 0 and a multiple of 8 */
+  int64_t V;                /* vocabulary size; > 0 */
+  int64_t ignore_index;     /* targets equal to this are ignored (any int64, default -100) */
+  float label_smoothing;    /* eps in [0, 1] */
+  float lse_square_scale;   /* lam >= 0 (z-loss) */
+  float logit_scale;        /* s, any finite value */
+  int32_t reduction;        /* flce_reduction_t */
+  int32_t has_bias;         /* 1: b is given ([V] bf16) */
+  int32_t dW_fp32;          /* backward: 1 = dW written as fp32, 0 = bf16 */
+  int32_t db_fp32;          /* backward: 1 = db written as fp32, 0 = bf16 */
+  int64_t bwd_vocab_block;  /* backward vocab block BVc (multiple of 256); 0 = library default */
+} flce_params_t;
+
+/* Workspace bytes a call needs: which = 0 for flce_forward, 1 for
+ * flce_backward. Returns 0 for invalid parameters or N == 0. */
+size_t flce_workspace_size(const flce_params_t* p, int which);
+
+/*
+ * Forward. x: [N, H] bf16; W: [V, H] bf16; b: [V] bf16 or NULL (has_bias = 0);
+ * y: [N] int64 targets in [0, V) or ignore_index.
+ * Writes loss (fp32, [1] for sum/mean, [N] for none) and lse ([N] fp32,
+ * natural log, for every token including ignored ones). lse is what
+ * flce_backward needs from the forward pass.
+ * x, W, b and the workspace must be 16-byte aligned. dev_err: one device
+ * int32 (may be NULL to skip device error reporting).
+ */
+flce_status_t flce_forward(const flce_params_t* p, const void* x, const void* W, const void* b,
+                           const int64_t* y, float* loss, float* lse, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_err, void* stream);
+
+/*
+ * Backward. dloss: device fp32, [1] for sum/mean or [N] for none (the
+ * gradient of the caller's objective with respect to `loss`). lse: the
+ * forward's [N] output. x, W, b, y as in flce_forward (the logits are
+ * recomputed from them one vocabulary block at a time).
+ * Writes dx [N, H] bf16, dW [V, H] (fp32 or bf16 per dW_fp32) and, when
+ * has_bias, db [V] (fp32 or bf16 per db_fp32). Every element of dx, dW and db
+ * is overwritten (no accumulation into the caller's buffers).
+ */
+flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const float* lse,
+                            const void* x, const void* W, const void* b, const int64_t* y,
+                            void* dx, void* dW, void* db, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_err, void* stream);
+
+/* Synchronises `stream`, reads the device error word into *host_err (HOST
+ * pointer, may be NULL), clears the device word and maps it to a status:
+ * FLCE_OK, FLCE_ERR_TARGET_OUT_OF_RANGE or FLCE_ERR_TIMEOUT. */
+flce_status_t flce_read_device_error(int32_t* dev_err, void* stream, int32_t* host_err);
+
+/* Static string for a status code. */
+const char* flce_status_string(flce_status_t status);
+
+/* Library version, e.g. "0.1.0". */
+const char* flce_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H_ */

@@ -1,0 +1,221 @@
+"""GB300 (sm_103a) fused linear cross-entropy.
+
+Python binding of the C ABI in ``include/flce.h``: the functions here only
+check and marshal arguments (device pointers, sizes, the current CUDA
+stream) and allocate outputs and workspace through PyTorch. Every step of the
+computation runs in the library's CUDA kernels; if the library is missing,
+calls raise instead of falling back to anything else.
+
+    loss, lse = flce_forward(x, W, b, y, reduction="mean")
+    dx, dW, db = flce_backward(dloss, lse, x, W, b, y, reduction="mean")
+
+The loss follows the fla ``FusedLinearCrossEntropyLoss`` options
+(ignore_index, label_smoothing, logit_scale, reduction) plus the z-loss
+``lse_square_scale`` of Liger-Kernel PR #239 and reduction "none" of
+DeepSpeed PR #8792.
+"""
+from __future__ import annotations
+
+from typing import Optional, Tuple
+
+import torch
+
+from . import _lib
+from ._lib import FlceError, params
+
+__all__ = [
+    "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
+    "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
+    "fused_linear_cross_entropy", "FlceError", "params",
+]
+
+_err_words = {}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def device_error_word(device) -> torch.Tensor:
+    """The int32 device word this binding passes as ``dev_err`` on ``device``."""
+    d = torch.device(device)
+    key = d.index if d.index is not None else torch.cuda.current_device()
+    w = _err_words.get(key)
+    if w is None:
+        w = torch.zeros(1, dtype=torch.int32, device=torch.device("cuda", key))
+        _err_words[key] = w
+    return w
+
+
+def _check_inputs(x, W, b, y):
+    if not (x.is_cuda and W.is_cuda and y.is_cuda):
+        raise ValueError("flce: x, W and y must be CUDA tensors")
+    if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
+        raise TypeError("flce: x and W must be bf16")
+    if b is not None and (b.dtype != torch.bfloat16 or not b.is_cuda):
+        raise TypeError("flce: b must be a bf16 CUDA tensor")
+    if y.dtype != torch.int64:
+        raise TypeError("flce: y must be int64")
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1] or y.shape != (x.shape[0],):
+        raise ValueError(f"flce: bad shapes x{tuple(x.shape)} W{tuple(W.shape)} y{tuple(y.shape)}")
+    if b is not None and b.shape != (W.shape[0],):
+        raise ValueError("flce: b must have shape [V]")
+    for t in (x, W, y) + ((b,) if b is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("flce: tensors must be contiguous")
+
+
+def flce_workspace_size(N, H, V, which: str, **opts) -> int:
+    p = params(N, H, V, **opts)
+    return int(_lib.load().flce_workspace_size(p, 0 if which == "forward" else 1))
+
+
+def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: torch.Tensor, *,
+                 ignore_index: int = -100, label_smoothing: float = 0.0,
+                 lse_square_scale: float = 0.0, logit_scale: float = 1.0,
+                 reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
+                 out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
+                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Loss and per-token lse. loss is a 0-dim fp32 tensor (sum/mean) or [N]
+    fp32 (none); lse is [N] fp32. Runs on the current stream, no sync."""
+    _check_inputs(x, W, b, y)
+    lib = _lib.load()
+    N, H = x.shape
+    V = W.shape[0]
+    p = params(N, H, V, ignore_index=ignore_index, label_smoothing=label_smoothing,
+               lse_square_scale=lse_square_scale, logit_scale=logit_scale,
+               reduction=reduction, has_bias=b is not None)
+    dev = x.device
+    if out is not None:
+        loss, lse = out
+    else:
+        loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=dev)
+        lse = torch.empty(N, dtype=torch.float32, device=dev)
+    need = lib.flce_workspace_size(p, 0)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.flce_forward(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse),
+                          _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
+                          _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_forward")
+    return (loss if reduction == "none" else loss.view(())), lse
+
+
+def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: torch.Tensor,
+                  b: Optional[torch.Tensor], y: torch.Tensor, *, ignore_index: int = -100,
+                  label_smoothing: float = 0.0, lse_square_scale: float = 0.0,
+                  logit_scale: float = 1.0, reduction: str = "mean",
+                  dW_dtype: torch.dtype = torch.float32, db_dtype: torch.dtype = torch.float32,
+                  bwd_vocab_block: int = 0, workspace: Optional[torch.Tensor] = None,
+                  out: Optional[Tuple] = None, stream=None):
+    """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None."""
+    _check_inputs(x, W, b, y)
+    lib = _lib.load()
+    N, H = x.shape
+    V = W.shape[0]
+    dev = x.device
+    dloss = dloss.reshape(-1)
+    if dloss.dtype != torch.float32 or not dloss.is_cuda or not dloss.is_contiguous():
+        raise TypeError("flce: dloss must be a contiguous fp32 CUDA tensor")
+    if dloss.numel() != (N if reduction == "none" else 1):
+        raise ValueError("flce: dloss must have N elements (none) or 1 (sum/mean)")
+    if lse.dtype != torch.float32 or lse.shape != (N,):
+        raise ValueError("flce: lse must be the forward's [N] fp32 output")
+    if dW_dtype not in (torch.float32, torch.bfloat16) or db_dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("flce: dW_dtype and db_dtype must be fp32 or bf16")
+    p = params(N, H, V, ignore_index=ignore_index, label_smoothing=label_smoothing,
+               lse_square_scale=lse_square_scale, logit_scale=logit_scale,
+               reduction=reduction, has_bias=b is not None,
+               dW_fp32=dW_dtype == torch.float32, db_fp32=db_dtype == torch.float32,
+               bwd_vocab_block=bwd_vocab_block)
+    if out is not None:
+        dx, dW, db = out
+    else:
+        dx = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        dW = torch.empty(V, H, dtype=dW_dtype, device=dev)
+        db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
+    need = lib.flce_workspace_size(p, 1)
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    st = lib.flce_backward(p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y),
+                           _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), workspace.numel(),
+                           _ptr(device_error_word(dev)), _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_backward")
+    return dx, dW, db
+
+
+def flce_read_device_error(device=None, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error bits
+    (FLCE_DEVERR_TARGET = 1, FLCE_DEVERR_TIMEOUT = 2) raised by earlier calls."""
+    import ctypes
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    h = ctypes.c_int32(0)
+    st = _lib.load().flce_read_device_error(_ptr(device_error_word(dev)), _stream(stream),
+                                           ctypes.byref(h))
+    if st not in (_lib.FLCE_OK, 4, 6):
+        raise FlceError(st, "flce_read_device_error")
+    return int(h.value)
+
+
+class FusedLinearCrossEntropyFunction(torch.autograd.Function):
+    """Autograd wrapper: forward keeps only lse; backward recomputes the logits."""
+
+    @staticmethod
+    def forward(ctx, x, target, weight, bias=None, ignore_index=-100, label_smoothing=0.0,
+                lse_square_scale=0.0, logit_scale=1.0, reduction="mean"):
+        loss, lse = flce_forward(x, weight, bias, target, ignore_index=ignore_index,
+                                 label_smoothing=label_smoothing,
+                                 lse_square_scale=lse_square_scale, logit_scale=logit_scale,
+                                 reduction=reduction)
+        ctx.save_for_backward(x, target, weight, bias, lse)
+        ctx.opts = dict(ignore_index=ignore_index, label_smoothing=label_smoothing,
+                        lse_square_scale=lse_square_scale, logit_scale=logit_scale,
+                        reduction=reduction)
+        return loss
+
+    @staticmethod
+    def backward(ctx, dloss):
+        x, target, weight, bias, lse = ctx.saved_tensors
+        dx, dW, db = flce_backward(dloss.float().contiguous(), lse, x, weight, bias, target,
+                                   dW_dtype=torch.float32, db_dtype=torch.float32, **ctx.opts)
+        dW = dW.to(weight.dtype)
+        db = None if db is None else db.to(bias.dtype)
+        return dx, None, dW, db, None, None, None, None, None
+
+
+def fused_linear_cross_entropy(x, target, weight, bias=None, ignore_index=-100,
+                               label_smoothing=0.0, lse_square_scale=0.0, logit_scale=1.0,
+                               reduction="mean"):
+    """Functional form; x [N, H] bf16, target [N] int64, weight [V, H] bf16."""
+    return FusedLinearCrossEntropyFunction.apply(x, target, weight, bias, ignore_index,
+                                                 label_smoothing, lse_square_scale,
+                                                 logit_scale, reduction)
+
+
+class FusedLinearCrossEntropyLoss(torch.nn.Module):
+    """Module form: flattens x [..., H] and target [...] to [N, H] and [N]."""
+
+    def __init__(self, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
+                 logit_scale=1.0, reduction="mean"):
+        super().__init__()
+        if reduction not in ("none", "sum", "mean"):
+            raise ValueError(f"reduction: {reduction} is not supported")
+        self.ignore_index = ignore_index
+        self.label_smoothing = label_smoothing
+        self.lse_square_scale = lse_square_scale
+        self.logit_scale = logit_scale
+        self.reduction = reduction
+
+    def forward(self, x, target, weight, bias=None):
+        return fused_linear_cross_entropy(
+            x.reshape(-1, x.shape[-1]).contiguous(), target.reshape(-1).contiguous(), weight,
+            bias, self.ignore_index, self.label_smoothing, self.lse_square_scale,
+            self.logit_scale, self.reduction)

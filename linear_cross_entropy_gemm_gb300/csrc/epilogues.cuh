@@ -1,0 +1,327 @@
+// Epilogues of the FLCE GEMMs. Each runs on the 128 epilogue threads of
+// gemm_persistent; thread i owns row i of the 128 x 256 fp32 accumulator in
+// TMEM and reads it 32 columns at a time.
+//
+// Notation (fla fused_linear_cross_entropy.py; Liger-Kernel PR #239):
+//   z = s * (acc + b_v)          logits of one token row, vocab column v
+//   lse = log sum_v exp(z_v)      kept per (row, vocab tile) as base-2 (m, d)
+//   dL = s * g * ((1 + 2 lam lse) p - eps/V - (1 - eps) [v == y]),  p = exp(z - lse)
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "gemm_engine.cuh"
+
+namespace flce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Bias of 32 consecutive vocab columns starting at col0 (< V); zero past V.
+template <bool HAS_BIAS>
+__device__ __forceinline__ void load_bias32(const __nv_bfloat16* __restrict__ bias, int col0, int V,
+                                            float (&bv)[32]) {
+  if constexpr (!HAS_BIAS) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) bv[j] = 0.f;
+  } else {
+    if (col0 + 32 <= V) {
+      const uint4* p = reinterpret_cast<const uint4*>(bias + col0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 u = __ldg(p + q);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          bv[q * 8 + 2 * e] = __uint_as_float(w[e] << 16);
+          bv[q * 8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) bv[j] = (col0 + j < V) ? __bfloat162float(bias[col0 + j]) : 0.f;
+    }
+  }
+}
+
+// Column sums of a 32 x 32 block held one row per lane: afterwards lane L
+// holds the sum over the warp of column L (recursive halving, 31 shuffles).
+__device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return v[0];
+}
+
+// ------------------------------------------------------------------ forward
+// Folds each logits tile into per-(row, vocab tile) base-2 online-softmax
+// partials (m = max z log2e, d = sum 2^(z log2e - m)), the tile's sum of z
+// (label smoothing only) and the target logit z_y when y falls in the tile.
+struct FwdLseArgs {
+  const __nv_bfloat16* bias;
+  const int64_t* y;
+  float scale;
+  int V;
+  int Ntok;
+  float* part_m;  // [tiles_v, Ntok]
+  float* part_d;  // [tiles_v, Ntok]
+  float* part_s;  // [tiles_v, Ntok] or null
+  float* zy;      // [Ntok]
+};
+
+template <bool HAS_BIAS, bool HAS_SMOOTH>
+struct FwdLseEpi {
+  static constexpr bool kAMN = false, kBMN = false;
+  using Args = FwdLseArgs;
+  __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
+                              int, int, uint32_t taddr) {
+    const int row = tm * kBM + row_in_tile;
+    const int v0 = tn * kBN;
+    const int64_t yv = row < a.Ntok ? __ldg(a.y + row) : -1;
+    const int ty = (yv >= v0 && yv < static_cast<int64_t>(v0) + kBN) ? static_cast<int>(yv - v0) : -1;
+    float m = -INFINITY, d = 0.f, S = 0.f, zt = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32], bv[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int col0 = v0 + c * 32;
+      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float z = (v[j] + bv[j]) * a.scale;
+        const bool ok = col0 + j < a.V;
+        if constexpr (HAS_SMOOTH) S += ok ? z : 0.f;
+        zt = (c * 32 + j == ty) ? z : zt;
+        v[j] = ok ? z * kLog2e : -INFINITY;
+        cm = fmaxf(cm, v[j]);
+      }
+      const float nm = fmaxf(m, cm);
+      if (nm != -INFINITY) {
+        float acc = d * fast_exp2(m - nm);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc += fast_exp2(v[j] - nm);
+        d = acc;
+        m = nm;
+      }
+    }
+    if (row < a.Ntok) {
+      const size_t o = static_cast<size_t>(tn) * a.Ntok + row;
+      a.part_m[o] = m;
+      a.part_d[o] = d;
+      if constexpr (HAS_SMOOTH) a.part_s[o] = S;
+      if (ty >= 0) a.zy[row] = zt;
+    }
+  }
+};
+
+// ------------------------------------------------- backward: recompute + dL
+// Recomputes a logits tile of the current vocab block, forms
+// dL = a_n p - c_n - t_n [v == y_n] with per-row coefficients
+// (lse2 = lse log2e, a = s g (1 + 2 lam lse), c = s g eps / V, t = s g (1 - eps)),
+// writes it as bf16 into the staged block dL[Ntok, ld] and, with a bias,
+// writes per-warp column sums (fp32, before rounding) for db.
+struct DlogitsArgs {
+  const __nv_bfloat16* bias;
+  const int64_t* y;
+  const float4* coef;  // [Ntok]: (lse2, a, c, t)
+  float scale;
+  int V;
+  int Ntok;
+  int v0;              // first vocab id of the block
+  int Vb;              // vocab ids in the block
+  __nv_bfloat16* dL;   // [Ntok, ld_dL], block-relative columns
+  int ld_dL;
+  float* db_part;      // [tiles_m * 4, ld_db] or null
+  int ld_db;
+};
+
+template <bool HAS_BIAS>
+struct DlogitsEpi {
+  static constexpr bool kAMN = false, kBMN = false;
+  using Args = DlogitsArgs;
+  __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
+                              int lane, int quad, uint32_t taddr) {
+    const int row = tm * kBM + row_in_tile;
+    const bool row_ok = row < a.Ntok;
+    const int vt0 = tn * kBN;  // block-relative
+    const int vg0 = a.v0 + vt0;
+    const float4 cf = row_ok ? __ldg(a.coef + row) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int64_t yv = row_ok ? __ldg(a.y + row) : -1;
+    const int ty = (yv >= vg0 && yv < static_cast<int64_t>(vg0) + kBN) ? static_cast<int>(yv - vg0) : -1;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32], bv[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int colb0 = vt0 + c * 32;
+      const int colg0 = vg0 + c * 32;
+      load_bias32<HAS_BIAS>(a.bias, colg0 < a.V ? colg0 : 0, a.V, bv);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float z = (v[j] + bv[j]) * a.scale;
+        const float p = fast_exp2(fmaf(z, kLog2e, -cf.x));
+        float dl = fmaf(cf.y, p, -cf.z);
+        dl -= (c * 32 + j == ty) ? cf.w : 0.f;
+        v[j] = (row_ok && colb0 + j < a.Vb) ? dl : 0.f;
+      }
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(a.dL + static_cast<size_t>(row) * a.ld_dL + colb0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+          u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+          u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+          u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+          dst[q] = u;
+        }
+      }
+      if constexpr (HAS_BIAS) {
+        const float colsum = warp_column_sums(v, lane);
+        if (colb0 + lane < a.Vb)
+          a.db_part[static_cast<size_t>(tm * 4 + quad) * a.ld_db + colb0 + lane] = colsum;
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------- backward: dW
+// dW[v0 + r, :] = sum_n dL[n, r] x[n, :] for block-relative vocab row r.
+struct DwArgs {
+  void* out;      // dW [V, ld] fp32 or bf16
+  int out_bf16;
+  int ld;         // H
+  int row0;       // v0
+  int Mrows;      // Vb
+  int Ncols;      // H
+};
+
+struct DwEpi {
+  static constexpr bool kAMN = true, kBMN = true;
+  using Args = DwArgs;
+  __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
+                              int, int, uint32_t taddr) {
+    const int r = tm * kBM + row_in_tile;
+    const bool row_ok = r < a.Mrows;
+    const size_t orow = static_cast<size_t>(a.row0 + (row_ok ? r : 0)) * a.ld;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int col0 = tn * kBN + c * 32;
+      if (row_ok && col0 < a.Ncols) store_dw(a, orow, col0, v);
+    }
+  }
+  __device__ static void store_dw(const Args& a, size_t orow, int col0, const float (&v)[32]) {
+    {
+      if (a.out_bf16) {
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + orow + col0;
+        if (col0 + 32 <= a.Ncols) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+            u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+            u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+            u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+            reinterpret_cast<uint4*>(o)[q] = u;
+          }
+        } else {
+          for (int j = 0; j < a.Ncols - col0; ++j) o[j] = __float2bfloat16_rn(v[j]);
+        }
+      } else {
+        float* o = reinterpret_cast<float*>(a.out) + orow + col0;
+        if (col0 + 32 <= a.Ncols) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(o)[q] =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          for (int j = 0; j < a.Ncols - col0; ++j) o[j] = v[j];
+        }
+      }
+    }
+  }
+};
+
+// ---------------------------------------------------------- backward: dx
+// dx[n, :] accumulates sum over vocab blocks of dL_block[n, :] W_block in an
+// fp32 buffer; the first block stores, the last one writes bf16 dx.
+struct DxArgs {
+  float* acc;             // [Ntok, ld] fp32 (unused when first && last)
+  __nv_bfloat16* out;     // dx [Ntok, ld] bf16
+  int ld;                 // H
+  int Ntok;
+  int Ncols;              // H
+  int first;
+  int last;
+};
+
+struct DxEpi {
+  static constexpr bool kAMN = false, kBMN = true;
+  using Args = DxArgs;
+  __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
+                              int, int, uint32_t taddr) {
+    const int row = tm * kBM + row_in_tile;
+    const bool row_ok = row < a.Ntok;
+    const size_t orow = static_cast<size_t>(row_ok ? row : 0) * a.ld;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int col0 = tn * kBN + c * 32;
+      if (row_ok && col0 < a.Ncols) accumulate(a, orow, col0, v);
+    }
+  }
+  __device__ static void accumulate(const Args& a, size_t orow, int col0, float (&v)[32]) {
+    {
+      const int ncol = min(32, a.Ncols - col0);
+      float* accp = a.acc + orow + col0;
+      if (ncol == 32) {
+        if (!a.first) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 p = reinterpret_cast<const float4*>(accp)[q];
+            v[4 * q] += p.x;
+            v[4 * q + 1] += p.y;
+            v[4 * q + 2] += p.z;
+            v[4 * q + 3] += p.w;
+          }
+        }
+        if (a.last) {
+          uint4* o = reinterpret_cast<uint4*>(a.out + orow + col0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
+            u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
+            u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
+            u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
+            o[q] = u;
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(accp)[q] =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      } else {
+        for (int j = 0; j < ncol; ++j) {
+          const float val = v[j] + (a.first ? 0.f : accp[j]);
+          if (a.last)
+            a.out[orow + col0 + j] = __float2bfloat16_rn(val);
+          else
+            accp[j] = val;
+        }
+      }
+    }
+  }
+};
+
+}  // namespace flce

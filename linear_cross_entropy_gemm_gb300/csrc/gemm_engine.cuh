@@ -1,0 +1,245 @@
+// Persistent, warp-specialised tcgen05 GEMM engine shared by every
+// contraction of the fused linear cross-entropy (FLCE) path.
+//
+//   D[M, N] = A[M, K] * B[N, K]^T   (bf16 in, fp32 accumulate in TMEM)
+//
+// One CTA per SM (192 threads):
+//   warp 0      TMA producer: a kStages-deep ring of (A, B) K-slices in smem
+//   warp 1      MMA issuer (one thread): tcgen05.mma 128x256x16 into one of
+//               two TMEM accumulators (2 x 256 fp32 columns = all 512)
+//   warps 2..5  epilogue: 128 threads, thread i owns accumulator row (TMEM
+//               lane) i; drains tile t while the MMAs of tile t+1 run
+// The tile loop is persistent (tile = blockIdx.x + j * gridDim.x), in an
+// order chosen per problem so the operand shared by concurrent CTAs stays in L2.
+//
+// Operands are 128-byte-swizzled bf16 tiles loaded by TMA, either K-major
+// (rows of 64 contiguous K elements) or MN-major (rows of 64 contiguous M/N
+// elements, one per K index); the tcgen05 instruction descriptor's transpose
+// bits select the form, so dW = dL^T x and dx = dL W need no transposed copies.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "sm103_primitives.cuh"
+
+namespace flce {
+
+constexpr int kBM = 128;      // accumulator rows (TMEM lanes)
+constexpr int kBN = 256;      // accumulator columns per buffer
+constexpr int kBK = 64;       // K elements per pipeline stage (one 128-B swizzle row)
+constexpr int kUmmaK = 16;    // K per tcgen05.mma (kind::f16)
+constexpr int kStages = 4;
+constexpr int kAStageBytes = kBM * kBK * 2;   // 16 KiB
+constexpr int kBStageBytes = kBN * kBK * 2;   // 32 KiB
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr int kTmemCols = 2 * kBN;
+constexpr int kMnBoxBytes = 64 * kBK * 2;     // one 64 (MN) x 64 (K) MN-major box
+constexpr int kBarrierBytes = 256;
+constexpr size_t kSmemBytes =
+    1024 + static_cast<size_t>(kStages) * (kAStageBytes + kBStageBytes) + kBarrierBytes;
+
+struct GemmGeom {
+  int M, N, K;
+  int tiles_m, tiles_n, k_blocks;
+  int a_mn_off, a_k_off;  // added to the A / B load coordinates
+  int b_mn_off, b_k_off;
+  int raster_m_inner;     // 1: consecutive tiles advance along M first
+  int group;              // >0: tiles walk M inner inside groups of `group` N-tiles
+};
+
+__device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, int& tn) {
+  if (g.group > 0) {
+    // Grouped raster: within a band of `group` N-tiles, walk M first.
+    const int band = g.group * g.tiles_m;
+    const int b = t / band;
+    const int r = t - b * band;
+    const int width = min(g.group, g.tiles_n - b * g.group);
+    tm = r / width;
+    tn = b * g.group + (r - tm * width);
+  } else if (g.raster_m_inner) {
+    tm = t % g.tiles_m;
+    tn = t / g.tiles_m;
+  } else {
+    tn = t % g.tiles_n;
+    tm = t / g.tiles_n;
+  }
+}
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return;
+  }
+}
+
+template <class Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_persistent(const __grid_constant__ CUtensorMap mapA,
+                    const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
+                    const typename Epi::Args ea, int* dev_err) {
+  constexpr bool kAMN = Epi::kAMN;
+  constexpr bool kBMN = Epi::kBMN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kAStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done_bar = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiThreads);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int num_tiles = g.tiles_m * g.tiles_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      const uint64_t pol = l2_policy_evict_normal();
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int tm, tn;
+        tile_coords(g, t, tm, tn);
+        const int m0 = tm * kBM, n0 = tn * kBN;
+        bool ok = true;
+        for (int kb = 0; kb < g.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, dev_err)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], kAStageBytes + kBStageBytes);
+          uint8_t* a = sA + s * kAStageBytes;
+          uint8_t* b = sB + s * kBStageBytes;
+          const int k0 = kb * kBK;
+          if constexpr (!kAMN) {
+            tma_load_2d(a, &mapA, &full[s], k0 + g.a_k_off, m0 + g.a_mn_off, pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j)
+              tma_load_2d(a + j * kMnBoxBytes, &mapA, &full[s], m0 + g.a_mn_off + j * 64,
+                          k0 + g.a_k_off, pol);
+          }
+          if constexpr (!kBMN) {
+            tma_load_2d(b, &mapB, &full[s], k0 + g.b_k_off, n0 + g.b_mn_off, pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBN / 64; ++j)
+              tma_load_2d(b + j * kMnBoxBytes, &mapB, &full[s], n0 + g.b_mn_off + j * 64,
+                          k0 + g.b_k_off, pol);
+          }
+          ++issued;
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: the last load issued into each stage must land before exit.
+      for (long long i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+        mbar_drain(&full[i % kStages], static_cast<uint32_t>((i / kStages) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // --------------------------------------------------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, kAMN, kBMN);
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t aph = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, dev_err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+        bool ok = true;
+        for (int kb = 0; kb < g.k_blocks; ++kb) {
+          if (!mbar_wait(&full[s], ph, abort_flag, dev_err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + s * kAStageBytes);
+          const uint32_t b_addr = smem_u32(sB + s * kBStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+            const uint64_t ad = kAMN ? smem_desc_sw128(a_addr + kk * (kUmmaK * 128), kMnBoxBytes, 1024)
+                                     : smem_desc_sw128(a_addr + kk * (kUmmaK * 2), 16, 1024);
+            const uint64_t bd = kBMN ? smem_desc_sw128(b_addr + kk * (kUmmaK * 128), kMnBoxBytes, 1024)
+                                     : smem_desc_sw128(b_addr + kk * (kUmmaK * 2), 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[s]);
+          if (++s == kStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        acc ^= 1;
+        if (acc == 0) aph ^= 1;
+      }
+      // Every MMA issued above must finish before TMEM is released.
+      umma_commit(done_bar);
+      mbar_drain(done_bar, 0);
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quad = warp & 3;  // TMEM lane quadrant this warp may access
+    const int row_in_tile = quad * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(g, t, tm, tn);
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, dev_err)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      Epi::tile(ea, g, tm, tn, row_in_tile, lane, quad, taddr);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+}  // namespace flce

@@ -1,0 +1,91 @@
+"""Helpers for GPU-vs-oracle parity: moving seeded inputs to the device,
+running the C ABI through the binding, and the tolerances.
+
+Tolerances (fixed for this method): loss and lse |got - ref| <= 1e-3 max(1,
+|ref|); dx, dW, db compared as fp32 with relative Frobenius error <= 5e-3 and
+max elementwise error <= 2^-7 max|ref|.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from linear_cross_entropy_gemm_gb300 import inputs as I
+
+LOSS_RTOL = 1e-3
+GRAD_FROB = 5e-3
+GRAD_MAX = 2.0 ** -7
+
+
+def bf16_dev(bits: np.ndarray, dev) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def opts_of(wl: I.Workload) -> dict:
+    return dict(ignore_index=wl.ignore_index, label_smoothing=wl.label_smoothing,
+                lse_square_scale=wl.lse_square_scale, logit_scale=wl.logit_scale,
+                reduction=wl.reduction)
+
+
+class DeviceProblem:
+    def __init__(self, inp: I.Inputs, dev="cuda:0"):
+        self.inp = inp
+        self.dev = torch.device(dev)
+        self.x = bf16_dev(inp.x, self.dev)
+        self.W = bf16_dev(inp.W, self.dev)
+        self.b = None if inp.b is None else bf16_dev(inp.b, self.dev)
+        self.y = torch.from_numpy(inp.y).to(self.dev)
+        self.dloss = torch.from_numpy(inp.dloss).to(self.dev)
+
+    def run(self, *, dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0, **over):
+        import linear_cross_entropy_gemm_gb300 as F
+        opts = opts_of(self.inp.wl)
+        opts.update(over)
+        loss, lse = F.flce_forward(self.x, self.W, self.b, self.y, **opts)
+        dx, dW, db = F.flce_backward(self.dloss, lse, self.x, self.W, self.b, self.y,
+                                     dW_dtype=dW_dtype, db_dtype=db_dtype,
+                                     bwd_vocab_block=bwd_vocab_block, **opts)
+        torch.cuda.synchronize(self.dev)
+        err = F.flce_read_device_error(self.dev)
+        return dict(loss=loss, lse=lse, dx=dx, dW=dW, db=db, err=err)
+
+
+def f64(inp: I.Inputs):
+    return (I.bf16_bits_to_f64(inp.x), I.bf16_bits_to_f64(inp.W),
+            None if inp.b is None else I.bf16_bits_to_f64(inp.b))
+
+
+def assert_loss_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64).reshape(-1)
+    ref = np.asarray(ref, dtype=np.float64).reshape(-1)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    err = np.abs(got - ref) / np.maximum(1.0, np.abs(ref))
+    i = int(np.argmax(err)) if err.size else 0
+    assert err.size == 0 or err[i] <= LOSS_RTOL, \
+        f"{what}: |d|/max(1,|ref|) = {err[i]:.3e} at {i} (got {got[i]!r}, ref {ref[i]!r})"
+
+
+def grad_errors(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    nref = np.linalg.norm(ref)
+    frob = np.linalg.norm(got - ref) / nref if nref > 0 else np.linalg.norm(got)
+    mref = np.max(np.abs(ref)) if ref.size else 0.0
+    mx = np.max(np.abs(got - ref)) if ref.size else 0.0
+    return frob, mx, mref
+
+
+def assert_grad_close(got, ref, what):
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    frob, mx, mref = grad_errors(got, ref)
+    if mref == 0.0:
+        assert mx == 0.0, f"{what}: expected exact zeros, max |got| {mx:.3e}"
+        return
+    assert frob <= GRAD_FROB and mx <= GRAD_MAX * mref, \
+        f"{what}: rel-Frobenius {frob:.3e} (<= {GRAD_FROB}), max err {mx:.3e} " \
+        f"(<= {GRAD_MAX * mref:.3e})"
+
+
+def to_np(t):
+    return None if t is None else t.detach().float().cpu().numpy()

@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every function include/flce.h
+declares; host-side argument checks return the documented statuses. No
+kernel is launched (these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_cross_entropy_gemm_gb300 import _lib
+from linear_cross_entropy_gemm_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "flce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _lib.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("flce_forward", "flce_backward", "flce_workspace_size",
+              "flce_read_device_error", "flce_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_params_struct_layout_matches_header():
+    assert ctypes.sizeof(_lib.FlceParams) == 72
+    assert _lib.FlceParams.bwd_vocab_block.offset == 64
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.flce_status_string(s)
+    assert lib.flce_version().decode().count(".") == 2
+
+
+def test_workspace_sizes(lib):
+    p = _lib.params(8192, 4096, 128256)
+    fwd = lib.flce_workspace_size(p, 0)
+    bwd = lib.flce_workspace_size(p, 1)
+    nt = (128256 + 255) // 256
+    assert fwd >= 2 * nt * 8192 * 4
+    assert bwd >= 8192 * 16384 * 2 + 8192 * 4096 * 4
+    ps = _lib.params(8192, 4096, 128256, label_smoothing=0.1)
+    assert lib.flce_workspace_size(ps, 0) >= fwd + nt * 8192 * 4
+    assert lib.flce_workspace_size(_lib.params(0, 64, 10), 0) == 0
+    assert lib.flce_workspace_size(_lib.params(4, 12, 10), 0) == 0  # H % 8 != 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=-1), 1), (dict(H=0), 1), (dict(V=0), 1), (dict(H=12), 2),
+    (dict(label_smoothing=1.5), 1), (dict(lse_square_scale=-1.0), 1),
+    (dict(bwd_vocab_block=100), 1),
+])
+def test_invalid_params_rejected_on_host(lib, kw, status):
+    base = dict(N=4, H=64, V=10)
+    base.update(kw)
+    N, H, V = base.pop("N"), base.pop("H"), base.pop("V")
+    p = _lib.params(N, H, V, **base)
+    fake = ctypes.c_void_p(4096)  # never dereferenced: rejected before any launch
+    st = lib.flce_forward(p, fake, fake, None, fake, fake, fake, fake, 1 << 30, None, None)
+    assert st == status
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    p = _lib.params(4, 64, 10)
+    f = ctypes.c_void_p(4096)
+    assert lib.flce_forward(p, None, f, None, f, f, f, f, 1 << 30, None, None) == 1
+    assert lib.flce_forward(p, ctypes.c_void_p(4098), f, None, f, f, f, f, 1 << 30, None,
+                            None) == 2
+    assert lib.flce_forward(p, f, f, None, f, f, f, f, 16, None, None) == 3
+    pb = _lib.params(4, 64, 10, has_bias=True)
+    assert lib.flce_forward(pb, f, f, None, f, f, f, f, 1 << 30, None, None) == 1
+    assert lib.flce_backward(p, None, f, f, f, None, f, f, f, None, f, 1 << 30, None,
+                             None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_lib, "_lib", None)
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        _lib.load()

@@ -1,0 +1,186 @@
+"""GPU parity: the sm_103a library (through its C ABI) against the CPU fp64
+oracle on identical seeded inputs.
+
+Small problems compare every output element; the full-size problems compare
+every token's loss and lse, 256 sampled token rows of dx and 256 sampled
+vocabulary rows of dW (and db). All tests need a GB300 (sm_103).
+"""
+import numpy as np
+import pytest
+import torch
+
+import linear_cross_entropy_gemm_gb300 as F
+from linear_cross_entropy_gemm_gb300 import inputs as I
+from oracle import flce_oracle as O
+from parity import (DeviceProblem, assert_grad_close, assert_loss_close, f64, opts_of, to_np)
+
+pytestmark = pytest.mark.gpu
+
+
+def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.float32):
+    inp = I.make_inputs(wl)
+    out = DeviceProblem(inp).run(bwd_vocab_block=bwd_vocab_block, dW_dtype=dW_dtype,
+                                 db_dtype=db_dtype)
+    assert out["err"] == 0, f"device error word {out['err']}"
+    x64, W64, b64 = f64(inp)
+    opts = opts_of(wl)
+    rl, rlse = O.forward(x64, W64, b64, inp.y, **opts)
+    rdx, rdW, rdb = O.backward(inp.dloss.astype(np.float64), x64, W64, b64, inp.y, **opts)
+    assert_loss_close(to_np(out["loss"]), rl, f"{wl.name} loss")
+    assert_loss_close(to_np(out["lse"]), rlse, f"{wl.name} lse")
+    assert_grad_close(to_np(out["dx"]), rdx, f"{wl.name} dx")
+    assert_grad_close(to_np(out["dW"]), rdW, f"{wl.name} dW")
+    if wl.has_bias:
+        assert_grad_close(to_np(out["db"]), rdb, f"{wl.name} db")
+    return out
+
+
+def test_tiny_full():
+    full_check(I.WORKLOADS["tiny"])
+
+
+def test_medium_full_with_bias_smoothing_zloss():
+    full_check(I.WORKLOADS["medium"])
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
+def test_ragged_tails_multi_block(reduction):
+    # N, H, V not multiples of the 128 x 256 x 64 tile; vocab blocks of 256
+    # leave a 1-column last block.
+    wl = I.Workload("ragged", N=129, H=72, V=257, seed=21, b_std=0.5, ignore_frac=0.1,
+                    label_smoothing=0.2, lse_square_scale=1e-2, logit_scale=1.3,
+                    reduction=reduction,
+                    dloss="normal_per_token" if reduction == "none" else "normal_scalar")
+    full_check(wl, bwd_vocab_block=256)
+
+
+def test_degenerate_single_class_single_token():
+    wl = I.Workload("v1", N=1, H=8, V=1, seed=22, b_std=1.0, label_smoothing=0.3,
+                    lse_square_scale=0.1, reduction="sum")
+    full_check(wl)
+
+
+def test_few_tokens_many_vocab_blocks():
+    wl = I.Workload("wide", N=5, H=64, V=5000, seed=23, x_std=2.0, w_std=0.1,
+                    label_smoothing=0.05, reduction="mean")
+    full_check(wl, bwd_vocab_block=1024)
+
+
+def test_bf16_gradients_and_custom_ignore_index():
+    wl = I.Workload("bf16out", N=200, H=128, V=777, seed=24, b_std=0.1, ignore_frac=0.2,
+                    ignore_index=5, reduction="mean")
+    full_check(wl, dW_dtype=torch.bfloat16, db_dtype=torch.bfloat16, bwd_vocab_block=512)
+
+
+def test_all_rows_ignored_mean_gives_zero():
+    wl = I.Workload("allign", N=64, H=64, V=300, seed=25, ignore_frac=1.0, reduction="mean",
+                    label_smoothing=0.1, lse_square_scale=1e-2)
+    out = full_check(wl)
+    assert float(out["loss"]) == 0.0
+    assert torch.count_nonzero(out["dx"]).item() == 0
+    assert torch.count_nonzero(out["dW"]).item() == 0
+
+
+def test_empty_batch():
+    dev = torch.device("cuda", 0)
+    x = torch.empty(0, 64, dtype=torch.bfloat16, device=dev)
+    W = torch.randn(100, 64, device=dev).to(torch.bfloat16)
+    y = torch.empty(0, dtype=torch.int64, device=dev)
+    loss, lse = F.flce_forward(x, W, None, y, reduction="mean")
+    dx, dW, _ = F.flce_backward(torch.ones(1, device=dev), lse, x, W, None, y)
+    torch.cuda.synchronize()
+    assert float(loss) == 0.0 and lse.numel() == 0 and dx.numel() == 0
+    assert torch.count_nonzero(dW).item() == 0
+
+
+def test_out_of_range_target_sets_device_error():
+    wl = I.Workload("badtarget", N=40, H=64, V=100, seed=26)
+    inp = I.make_inputs(wl)
+    inp.y[3] = 100   # == V
+    inp.y[7] = -5    # negative, not ignore_index
+    out = DeviceProblem(inp).run()
+    assert out["err"] & 1, "target error bit not raised"
+    assert F.flce_read_device_error() == 0, "error word not cleared"
+
+
+def test_run_to_run_bitwise_determinism():
+    wl = I.WORKLOADS["medium"].with_(N=1000, V=3000)
+    p = DeviceProblem(I.make_inputs(wl))
+    a = p.run(bwd_vocab_block=1024)
+    b = p.run(bwd_vocab_block=1024)
+    for k in ("loss", "lse", "dx", "dW", "db"):
+        assert torch.equal(a[k], b[k]), f"{k} differs between runs"
+
+
+def test_autograd_module_matches_c_abi():
+    wl = I.Workload("module", N=256, H=128, V=1000, seed=27, b_std=0.05, ignore_frac=0.05,
+                    label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.9)
+    inp = I.make_inputs(wl)
+    p = DeviceProblem(inp)
+    ref = p.run()
+    x = p.x.clone().requires_grad_(True)
+    W = p.W.clone().requires_grad_(True)
+    b = p.b.clone().requires_grad_(True)
+    mod = F.FusedLinearCrossEntropyLoss(label_smoothing=0.1, lse_square_scale=1e-3,
+                                        logit_scale=0.9)
+    loss = mod(x.view(2, 128, 128), p.y.view(2, 128), W, b)
+    loss.backward()
+    torch.cuda.synchronize()
+    assert torch.equal(loss.detach().reshape(1), ref["loss"].reshape(1))
+    assert torch.equal(x.grad, ref["dx"])
+    assert torch.equal(W.grad, ref["dW"].to(torch.bfloat16))
+    assert torch.equal(b.grad, ref["db"].to(torch.bfloat16))
+
+
+# ------------------------------------------------------------ full sizes
+
+_cache = {}
+
+
+def _sampled(name):
+    """GPU outputs plus the oracle on every token's statistics, 256 sampled
+    dx rows and 256 sampled dW / db rows, for one full-size problem."""
+    if name in _cache:
+        return _cache[name]
+    _cache.clear()
+    wl = I.WORKLOADS[name]
+    inp = I.make_inputs(wl)
+    out = DeviceProblem(inp).run()
+    assert out["err"] == 0, f"device error word {out['err']}"
+    opts = opts_of(wl)
+    x64, W64, b64 = f64(inp)
+    lse, zt, sz = O.row_stats(x64, W64, b64, inp.y, ignore_index=wl.ignore_index,
+                              logit_scale=wl.logit_scale, block=256)
+    tl = O.token_losses_from_stats(lse, zt, sz, inp.y, wl.V, wl.ignore_index,
+                                   wl.label_smoothing, wl.lse_square_scale)
+    ref_loss = O.reduce_losses(tl, inp.y, wl.ignore_index, wl.reduction)
+    ignored = np.nonzero(inp.y == wl.ignore_index)[0][:8]
+    rows = I.sample_indices(wl.seed, wl.N, 256, must_include=list(ignored) + [0, wl.N - 1])
+    valid_y = inp.y[inp.y != wl.ignore_index]
+    top = np.argsort(-np.bincount(valid_y, minlength=wl.V))[:8] if valid_y.size else []
+    edges = [0, 1, 255, 256, 16383, 16384, wl.V - 256, wl.V - 1]
+    vrows = I.sample_indices(wl.seed + 1, wl.V, 256, must_include=list(top) + edges)
+    dl = inp.dloss.astype(np.float64)
+    rdx = O.dx_rows(rows, dl, x64, W64, b64, inp.y, **opts)
+    rdW, rdb = O.dW_db_rows(vrows, lse, dl, x64, W64, b64, inp.y, **opts)
+    got = dict(loss=to_np(out["loss"]), lse=to_np(out["lse"]),
+               dx=to_np(out["dx"][torch.from_numpy(rows).to(out["dx"].device)]),
+               dW=to_np(out["dW"][torch.from_numpy(vrows).to(out["dW"].device)]),
+               db=None if out["db"] is None else to_np(out["db"])[vrows])
+    del out
+    torch.cuda.empty_cache()
+    res = dict(wl=wl, got=got, ref=dict(loss=ref_loss, lse=lse, dx=rdx, dW=rdW, db=rdb))
+    _cache[name] = res
+    return res
+
+
+@pytest.mark.parametrize("name", ["llama3_head", "large_logit", "vocab256k"])
+def test_full_size_sampled(name):
+    r = _sampled(name)
+    g, ref, wl = r["got"], r["ref"], r["wl"]
+    assert_loss_close(g["loss"], ref["loss"], f"{name} loss")
+    assert_loss_close(g["lse"], ref["lse"], f"{name} lse (all tokens)")
+    assert_grad_close(g["dx"], ref["dx"], f"{name} dx (sampled rows)")
+    assert_grad_close(g["dW"], ref["dW"], f"{name} dW (sampled vocab rows)")
+    if wl.has_bias:
+        assert_grad_close(g["db"], ref["db"], f"{name} db (sampled)")
