@@ -85,6 +85,32 @@ typedef struct {
   int64_t bwd_vocab_block;  /* backward vocab block BVc (multiple of 256); 0 = library default */
 } flce_params_t;
 
+/* Kernel kinds reported by the traced entry points. */
+typedef enum {
+  FLCE_KERNEL_FWD_LSE = 0,      /* forward GEMM + online-softmax partials */
+  FLCE_KERNEL_FWD_MERGE = 1,    /* partial merge -> lse, per-token loss */
+  FLCE_KERNEL_FWD_FINALIZE = 2, /* ordered sum of the loss (sum / mean) */
+  FLCE_KERNEL_BWD_PREP = 3,     /* per-token backward coefficients */
+  FLCE_KERNEL_BWD_DLOGITS = 4,  /* recompute a vocab block's logits -> bf16 dL */
+  FLCE_KERNEL_BWD_DB = 5,       /* bias-gradient partial sum of a block */
+  FLCE_KERNEL_BWD_DW = 6,       /* dW block GEMM */
+  FLCE_KERNEL_BWD_DX = 7        /* dx accumulate GEMM */
+} flce_kernel_t;
+
+/* Optional per-kernel timing without a profiler. The caller creates
+ * `capacity` CUDA events (cudaEvent_t, passed as void*) and an int32 array
+ * `kinds` of the same length. A traced call records events[0] on `stream`
+ * before its first launch and events[i + 1] right after launch i, whose
+ * flce_kernel_t it stores in kinds[i]; `count` returns the events recorded
+ * (recording stops silently at capacity). Elapsed time between events i and
+ * i + 1 is launch i's time on the stream. The library keeps no reference. */
+typedef struct {
+  void** events;
+  int32_t capacity;
+  int32_t count;
+  int32_t* kinds;
+} flce_trace_t;
+
 /* Workspace bytes a call needs: which = 0 for flce_forward, 1 for
  * flce_backward. Returns 0 for invalid parameters or N == 0. */
 size_t flce_workspace_size(const flce_params_t* p, int which);
@@ -115,6 +141,17 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
                             const void* x, const void* W, const void* b, const int64_t* y,
                             void* dx, void* dW, void* db, void* workspace, size_t workspace_bytes,
                             int32_t* dev_err, void* stream);
+
+/* flce_forward / flce_backward with an optional trace (NULL = untraced). */
+flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const void* W,
+                                  const void* b, const int64_t* y, float* loss, float* lse,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                  void* stream, flce_trace_t* trace);
+flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, const float* lse,
+                                   const void* x, const void* W, const void* b, const int64_t* y,
+                                   void* dx, void* dW, void* db, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                   flce_trace_t* trace);
 
 /* Synchronises `stream`, reads the device error word into *host_err (HOST
  * pointer, may be NULL), clears the device word and maps it to a status:

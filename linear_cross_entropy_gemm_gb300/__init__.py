@@ -26,7 +26,7 @@ from ._lib import FlceError, params
 __all__ = [
     "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
     "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
-    "fused_linear_cross_entropy", "FlceError", "params",
+    "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace",
 ]
 
 _err_words = {}
@@ -71,6 +71,29 @@ def _check_inputs(x, W, b, y):
             raise ValueError("flce: tensors must be contiguous")
 
 
+class KernelTrace:
+    """Caller-owned CUDA events for the traced entry points: after a traced
+    call, ``launches()`` gives (kernel name, milliseconds) per launch, timed
+    on the launching stream (flce_trace_t in include/flce.h)."""
+
+    def __init__(self, capacity: int = 256):
+        import ctypes
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.events:  # materialise the underlying cudaEvent_t
+            e.record()
+        self._handles = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.events])
+        self._kinds = (ctypes.c_int32 * capacity)()
+        self.struct = _lib.FlceTrace(ctypes.cast(self._handles, ctypes.POINTER(ctypes.c_void_p)),
+                                     capacity, 0,
+                                     ctypes.cast(self._kinds, ctypes.POINTER(ctypes.c_int32)))
+
+    def launches(self):
+        """Call after the stream has been synchronised."""
+        n = self.struct.count
+        return [(_lib.KERNEL_NAMES[self._kinds[i]], self.events[i].elapsed_time(self.events[i + 1]))
+                for i in range(n - 1)]
+
+
 def flce_workspace_size(N, H, V, which: str, **opts) -> int:
     p = params(N, H, V, **opts)
     return int(_lib.load().flce_workspace_size(p, 0 if which == "forward" else 1))
@@ -81,7 +104,7 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
                  lse_square_scale: float = 0.0, logit_scale: float = 1.0,
                  reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
                  out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
-                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 stream=None, trace: Optional[KernelTrace] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss and per-token lse. loss is a 0-dim fp32 tensor (sum/mean) or [N]
     fp32 (none); lse is [N] fp32. Runs on the current stream, no sync."""
     _check_inputs(x, W, b, y)
@@ -100,9 +123,9 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     need = lib.flce_workspace_size(p, 0)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    st = lib.flce_forward(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse),
-                          _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
-                          _stream(stream))
+    args = (p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse), _ptr(workspace),
+            workspace.numel(), _ptr(device_error_word(dev)), _stream(stream))
+    st = lib.flce_forward(*args) if trace is None else lib.flce_forward_traced(*args, trace.struct)
     if st != _lib.FLCE_OK:
         raise FlceError(st, "flce_forward")
     return (loss if reduction == "none" else loss.view(())), lse
@@ -114,7 +137,7 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                   logit_scale: float = 1.0, reduction: str = "mean",
                   dW_dtype: torch.dtype = torch.float32, db_dtype: torch.dtype = torch.float32,
                   bwd_vocab_block: int = 0, workspace: Optional[torch.Tensor] = None,
-                  out: Optional[Tuple] = None, stream=None):
+                  out: Optional[Tuple] = None, stream=None, trace: Optional[KernelTrace] = None):
     """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
@@ -144,9 +167,10 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
     need = lib.flce_workspace_size(p, 1)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    st = lib.flce_backward(p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y),
-                           _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), workspace.numel(),
-                           _ptr(device_error_word(dev)), _stream(stream))
+    args = (p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW),
+            _ptr(db), _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
+            _stream(stream))
+    st = lib.flce_backward(*args) if trace is None else lib.flce_backward_traced(*args, trace.struct)
     if st != _lib.FLCE_OK:
         raise FlceError(st, "flce_backward")
     return dx, dW, db

@@ -40,6 +40,20 @@ class FlceParams(ctypes.Structure):
     ]
 
 
+class FlceTrace(ctypes.Structure):
+    """Mirror of flce_trace_t."""
+    _fields_ = [
+        ("events", ctypes.POINTER(ctypes.c_void_p)),
+        ("capacity", ctypes.c_int32),
+        ("count", ctypes.c_int32),
+        ("kinds", ctypes.POINTER(ctypes.c_int32)),
+    ]
+
+
+KERNEL_NAMES = ("fwd_lse", "fwd_merge", "fwd_finalize", "bwd_prep", "bwd_dlogits", "bwd_db",
+                "bwd_dw", "bwd_dx")
+
+
 class FlceError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
@@ -68,6 +82,11 @@ def load() -> ctypes.CDLL:
     lib.flce_forward.restype = ctypes.c_int
     lib.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.flce_backward.restype = ctypes.c_int
+    T = ctypes.POINTER(FlceTrace)
+    lib.flce_forward_traced.argtypes = lib.flce_forward.argtypes + [T]
+    lib.flce_forward_traced.restype = ctypes.c_int
+    lib.flce_backward_traced.argtypes = lib.flce_backward.argtypes + [T]
+    lib.flce_backward_traced.restype = ctypes.c_int
     lib.flce_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.flce_read_device_error.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]

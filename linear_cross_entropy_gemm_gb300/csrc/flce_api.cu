@@ -172,6 +172,28 @@ int grid_for(const GemmGeom& g, int sms) {
   return tiles < sms ? tiles : sms;
 }
 
+// Records the caller's events around each launch (flce_trace_t in flce.h).
+struct Tracer {
+  flce_trace_t* t;
+  cudaStream_t s;
+  bool begin() {
+    if (!t) return true;
+    t->count = 0;
+    if (!t->events || t->capacity < 1) return true;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(t->events[0]), s) != cudaSuccess) return false;
+    t->count = 1;
+    return true;
+  }
+  bool after(flce_kernel_t kind) {
+    if (!t || t->count == 0 || t->count >= t->capacity) return true;
+    if (t->kinds) t->kinds[t->count - 1] = kind;
+    if (cudaEventRecord(static_cast<cudaEvent_t>(t->events[t->count]), s) != cudaSuccess)
+      return false;
+    ++t->count;
+    return true;
+  }
+};
+
 }  // namespace
 
 extern "C" {
@@ -192,6 +214,14 @@ size_t flce_workspace_size(const flce_params_t* p, int which) {
 flce_status_t flce_forward(const flce_params_t* p, const void* x, const void* W, const void* b,
                            const int64_t* y, float* loss, float* lse, void* workspace,
                            size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  return flce_forward_traced(p, x, W, b, y, loss, lse, workspace, workspace_bytes, dev_err,
+                             stream, nullptr);
+}
+
+flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const void* W,
+                                  const void* b, const int64_t* y, float* loss, float* lse,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                  void* stream, flce_trace_t* trace) {
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
   if (!loss) return FLCE_ERR_INVALID_ARG;
@@ -217,6 +247,8 @@ flce_status_t flce_forward(const flce_params_t* p, const void* x, const void* W,
       !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, kBN))
     return FLCE_ERR_CUDA;
 
+  Tracer tr{trace, s};
+  if (!tr.begin()) return FLCE_ERR_CUDA;
   GemmGeom g = geom(N, V, H);
   FwdLseArgs ea;
   ea.bias = static_cast<const __nv_bfloat16*>(p->has_bias ? b : nullptr);
@@ -229,7 +261,8 @@ flce_status_t flce_forward(const flce_params_t* p, const void* x, const void* W,
   ea.part_s = w.part_s;
   ea.zy = w.zy;
   if (launch_fwd_lse(mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
-                     reinterpret_cast<int*>(dev_err), grid_for(g, sms), s) != cudaSuccess)
+                     reinterpret_cast<int*>(dev_err), grid_for(g, sms), s) != cudaSuccess ||
+      !tr.after(FLCE_KERNEL_FWD_LSE))
     return FLCE_ERR_CUDA;
 
   MergeArgs ma;
@@ -250,7 +283,10 @@ flce_status_t flce_forward(const flce_params_t* p, const void* x, const void* W,
   ma.blk_sum = w.blk_sum;
   ma.blk_cnt = w.blk_cnt;
   ma.dev_err = reinterpret_cast<int*>(dev_err);
-  if (launch_merge(ma, s) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (launch_merge(ma, s) != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_MERGE)) return FLCE_ERR_CUDA;
+  if (p->reduction != FLCE_REDUCTION_NONE &&
+      (launch_finalize(ma, s) != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_FINALIZE)))
+    return FLCE_ERR_CUDA;
   return FLCE_OK;
 }
 
@@ -258,6 +294,15 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
                             const void* x, const void* W, const void* b, const int64_t* y,
                             void* dx, void* dW, void* db, void* workspace, size_t workspace_bytes,
                             int32_t* dev_err, void* stream) {
+  return flce_backward_traced(p, dloss, lse, x, W, b, y, dx, dW, db, workspace, workspace_bytes,
+                              dev_err, stream, nullptr);
+}
+
+flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, const float* lse,
+                                   const void* x, const void* W, const void* b, const int64_t* y,
+                                   void* dx, void* dW, void* db, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                   flce_trace_t* trace) {
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
   if (!dW || (p->has_bias && !db)) return FLCE_ERR_INVALID_ARG;
@@ -287,6 +332,8 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
   const int nblk = cdiv(V, bv);
   int* derr = reinterpret_cast<int*>(dev_err);
 
+  Tracer tr{trace, s};
+  if (!tr.begin()) return FLCE_ERR_CUDA;
   PrepArgs pa;
   pa.dloss = dloss;
   pa.lse = lse;
@@ -300,7 +347,7 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
   pa.reduction = p->reduction;
   pa.coef = w.coef;
   pa.dev_err = derr;
-  if (launch_prep(pa, s) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (launch_prep(pa, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_PREP)) return FLCE_ERR_CUDA;
 
   CUtensorMap mx_k, mw_k, mx_mn, mw_mn;
   if (!encode_2d(&mx_k, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM) ||
@@ -334,11 +381,13 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
     da.db_part = w.db_part;
     da.ld_db = static_cast<int>(bv);
     if (launch_dlogits(mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms), s) !=
-        cudaSuccess)
+            cudaSuccess ||
+        !tr.after(FLCE_KERNEL_BWD_DLOGITS))
       return FLCE_ERR_CUDA;
     if (p->has_bias &&
-        launch_db_finalize(w.db_part, g1.tiles_m * 4, static_cast<int>(bv), v0, Vb, db,
-                           p->db_fp32 != 0, s) != cudaSuccess)
+        (launch_db_finalize(w.db_part, g1.tiles_m * 4, static_cast<int>(bv), v0, Vb, db,
+                            p->db_fp32 != 0, s) != cudaSuccess ||
+         !tr.after(FLCE_KERNEL_BWD_DB)))
       return FLCE_ERR_CUDA;
 
     // dW block: one GEMM over all tokens (M = vocab rows, K = tokens).
@@ -351,7 +400,8 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
     wa.row0 = v0;
     wa.Mrows = Vb;
     wa.Ncols = H;
-    if (launch_dw(mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess)
+    if (launch_dw(mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
+        !tr.after(FLCE_KERNEL_BWD_DW))
       return FLCE_ERR_CUDA;
 
     // dx += dL_blk W_blk (K = the block's vocab rows).
@@ -366,7 +416,8 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
     xa.Ncols = H;
     xa.first = blk == 0;
     xa.last = blk == nblk - 1;
-    if (launch_dx(mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess)
+    if (launch_dx(mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess ||
+        !tr.after(FLCE_KERNEL_BWD_DX))
       return FLCE_ERR_CUDA;
   }
   return FLCE_OK;

@@ -46,6 +46,7 @@ struct MergeArgs {
 };
 constexpr int kMergeThreads = 256;
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st);
+cudaError_t launch_finalize(const MergeArgs& a, cudaStream_t st);
 
 struct PrepArgs {
   const float* dloss;

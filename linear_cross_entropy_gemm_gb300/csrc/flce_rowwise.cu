@@ -110,8 +110,11 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st) {
     merge_kernel<true><<<blocks, kMergeThreads, 0, st>>>(a);
   else
     merge_kernel<false><<<blocks, kMergeThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.reduction == 0) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const MergeArgs& a, cudaStream_t st) {
+  const int blocks = (a.N + kMergeThreads - 1) / kMergeThreads;
   finalize_loss_kernel<<<1, 1024, 0, st>>>(a.blk_sum, a.blk_cnt, blocks, a.reduction, a.loss);
   return cudaGetLastError();
 }
