@@ -153,6 +153,32 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
                                    size_t workspace_bytes, int32_t* dev_err, void* stream,
                                    flce_trace_t* trace);
 
+/*
+ * Forward without a workspace argument, for callers that cannot allocate
+ * device memory where they compute the loss (an inference-engine plugin whose
+ * enqueue step must not allocate, a service loop that forbids allocation
+ * after start-up, a component beside a caching allocator that holds nearly all
+ * device memory). The pages have no counterpart: this is a packaging of
+ * flce_forward, not part of the method.
+ *
+ * Arguments and results are those of flce_forward; the scratch that
+ * flce_forward takes from `workspace` comes instead from one array of
+ * FLCE_NOALLOC_SCRATCH_BYTES built into the library as a static device
+ * variable (every GPU that loads the library keeps it until the process
+ * exits). A problem whose flce_workspace_size(p, 0) exceeds that size is
+ * rejected with FLCE_ERR_WORKSPACE_TOO_SMALL before anything runs.
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.
+ * The call allocates and frees nothing. All calls share the one array, so
+ * calls that overlap on the GPU (e.g. on two streams) race on it: order them.
+ * Each call writes every scratch value it later reads, so stale contents from
+ * an earlier call never leak into a result.
+ */
+#define FLCE_NOALLOC_SCRATCH_BYTES (64 * 1024 * 1024)
+flce_status_t flce_forward_noalloc(const flce_params_t* p, const void* x, const void* W,
+                                   const void* b, const int64_t* y, float* loss, float* lse,
+                                   int32_t* dev_err, void* stream);
+
 /* Synchronises `stream`, reads the device error word into *host_err (HOST
  * pointer, may be NULL), clears the device word and maps it to a status:
  * FLCE_OK, FLCE_ERR_TARGET_OUT_OF_RANGE or FLCE_ERR_TIMEOUT. */
