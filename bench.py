@@ -310,6 +310,7 @@ def run_ours(args):
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "flushed (256 MiB write) before each timed step, outside the events",
                    "bwd_vocab_block": 16384, "dW_dtype": "fp32",
+                   "gemm": "cta pair" if os.environ.get("FLCE_CTA_PAIR", "1") != "0" else "single cta",
                    "N": N, "H": H, "V": V},
         "tflops_8nhv": tflops, "frac_bf16_peak_8nhv": tflops / pk["bf16_sus"],
         "tflops_6nhv_useful": tflops * 0.75,
@@ -334,10 +335,10 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=128)
+    ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="N,H,V override (profiling captures only)")

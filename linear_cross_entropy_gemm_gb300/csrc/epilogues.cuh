@@ -218,7 +218,8 @@ struct DwEpi {
       if (row_ok && col0 < a.Ncols) store_dw(a, orow, col0, v);
     }
   }
-  __device__ static void store_dw(const Args& a, size_t orow, int col0, const float (&v)[32]) {
+  __device__ __forceinline__ static void store_dw(const Args& a, size_t orow, int col0,
+                                                 const float (&v)[32]) {
     {
       if (a.out_bf16) {
         __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + orow + col0;
@@ -233,7 +234,9 @@ struct DwEpi {
             reinterpret_cast<uint4*>(o)[q] = u;
           }
         } else {
-          for (int j = 0; j < a.Ncols - col0; ++j) o[j] = __float2bfloat16_rn(v[j]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < a.Ncols - col0) o[j] = __float2bfloat16_rn(v[j]);
         }
       } else {
         float* o = reinterpret_cast<float*>(a.out) + orow + col0;
@@ -243,7 +246,9 @@ struct DwEpi {
             reinterpret_cast<float4*>(o)[q] =
                 make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
-          for (int j = 0; j < a.Ncols - col0; ++j) o[j] = v[j];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < a.Ncols - col0) o[j] = v[j];
         }
       }
     }
@@ -279,7 +284,8 @@ struct DxEpi {
       if (row_ok && col0 < a.Ncols) accumulate(a, orow, col0, v);
     }
   }
-  __device__ static void accumulate(const Args& a, size_t orow, int col0, float (&v)[32]) {
+  __device__ __forceinline__ static void accumulate(const Args& a, size_t orow, int col0,
+                                                   float (&v)[32]) {
     {
       const int ncol = min(32, a.Ncols - col0);
       float* accp = a.acc + orow + col0;
@@ -312,12 +318,15 @@ struct DxEpi {
                 make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         }
       } else {
-        for (int j = 0; j < ncol; ++j) {
-          const float val = v[j] + (a.first ? 0.f : accp[j]);
-          if (a.last)
-            a.out[orow + col0 + j] = __float2bfloat16_rn(val);
-          else
-            accp[j] = val;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          if (j < ncol) {
+            const float val = v[j] + (a.first ? 0.f : accp[j]);
+            if (a.last)
+              a.out[orow + col0 + j] = __float2bfloat16_rn(val);
+            else
+              accp[j] = val;
+          }
         }
       }
     }

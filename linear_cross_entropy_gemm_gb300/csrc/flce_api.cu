@@ -14,6 +14,7 @@
 //     dx GEMM       dx (+)= dL_blk W_blk                  (fp32 across blocks)
 //     db finalize   (with a bias)
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -63,6 +64,16 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 }
 
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+// GEMM kernel form: CTA pairs (cta_group::2, 256 x 256 tiles) or single CTAs
+// (128 x 256 tiles). FLCE_CTA_PAIR=0 / 1 in the environment overrides the
+// default; both forms compute identical results up to accumulation order.
+bool use_cta_pair() {
+  const char* e = std::getenv("FLCE_CTA_PAIR");
+  if (e && e[0] == '0') return false;
+  if (e && e[0] == '1') return true;
+  return true;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -242,9 +253,10 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
   carve_fwd(p, workspace, &w);
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
+  const bool pair = use_cta_pair();
   CUtensorMap mx, mw;
   if (!encode_2d(&mx, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM) ||
-      !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, kBN))
+      !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN))
     return FLCE_ERR_CUDA;
 
   Tracer tr{trace, s};
@@ -260,7 +272,7 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
   ea.part_d = w.part_d;
   ea.part_s = w.part_s;
   ea.zy = w.zy;
-  if (launch_fwd_lse(mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
+  if (launch_fwd_lse(pair, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
                      reinterpret_cast<int*>(dev_err), grid_for(g, sms), s) != cudaSuccess ||
       !tr.after(FLCE_KERNEL_FWD_LSE))
     return FLCE_ERR_CUDA;
@@ -331,6 +343,7 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
   const int64_t bv = vocab_block(p);
   const int nblk = cdiv(V, bv);
   int* derr = reinterpret_cast<int*>(dev_err);
+  const bool pair = use_cta_pair();
 
   Tracer tr{trace, s};
   if (!tr.begin()) return FLCE_ERR_CUDA;
@@ -351,7 +364,7 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
 
   CUtensorMap mx_k, mw_k, mx_mn, mw_mn;
   if (!encode_2d(&mx_k, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM) ||
-      !encode_2d(&mw_k, W, H, V, static_cast<uint64_t>(H) * 2, kBK, kBN) ||
+      !encode_2d(&mw_k, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN) ||
       !encode_2d(&mx_mn, x, H, N, static_cast<uint64_t>(H) * 2, 64, kBK) ||
       !encode_2d(&mw_mn, W, H, V, static_cast<uint64_t>(H) * 2, 64, kBK))
     return FLCE_ERR_CUDA;
@@ -380,7 +393,7 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
     da.ld_dL = static_cast<int>(bv);
     da.db_part = w.db_part;
     da.ld_db = static_cast<int>(bv);
-    if (launch_dlogits(mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms), s) !=
+    if (launch_dlogits(pair, mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms), s) !=
             cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DLOGITS))
       return FLCE_ERR_CUDA;
@@ -400,7 +413,7 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
     wa.row0 = v0;
     wa.Mrows = Vb;
     wa.Ncols = H;
-    if (launch_dw(mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
+    if (launch_dw(pair, mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DW))
       return FLCE_ERR_CUDA;
 
@@ -416,7 +429,7 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
     xa.Ncols = H;
     xa.first = blk == 0;
     xa.last = blk == nblk - 1;
-    if (launch_dx(mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess ||
+    if (launch_dx(pair, mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DX))
       return FLCE_ERR_CUDA;
   }

@@ -15,16 +15,18 @@ struct DlogitsArgs;
 struct DwArgs;
 struct DxArgs;
 
-// Persistent tcgen05 GEMMs (flce_gemm.cu). `grid` is the CTA count.
-cudaError_t launch_fwd_lse(const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
-                           const FwdLseArgs& ea, bool has_bias, bool has_smooth, int* dev_err,
+// Persistent tcgen05 GEMMs (flce_gemm.cu). pair = CTA-pair kernel (256 x 256
+// tiles; a K-major B map must then have 128-row boxes). `grid` is the CTA
+// count of the single-CTA kernel (the SM count when it is the smaller).
+cudaError_t launch_fwd_lse(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                           const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
+                           bool has_smooth, int* dev_err, int grid, cudaStream_t st);
+cudaError_t launch_dlogits(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                           const GemmGeom& g, const DlogitsArgs& ea, bool has_bias, int* dev_err,
                            int grid, cudaStream_t st);
-cudaError_t launch_dlogits(const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
-                           const DlogitsArgs& ea, bool has_bias, int* dev_err, int grid,
-                           cudaStream_t st);
-cudaError_t launch_dw(const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+cudaError_t launch_dw(bool pair, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                       const DwArgs& ea, int* dev_err, int grid, cudaStream_t st);
-cudaError_t launch_dx(const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+cudaError_t launch_dx(bool pair, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                       const DxArgs& ea, int* dev_err, int grid, cudaStream_t st);
 
 // Row-wise kernels (flce_rowwise.cu).

@@ -242,4 +242,209 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// ===========================================================================
+// CTA-pair variant (cluster of 2, tcgen05 cta_group::2): one 256 x 256 tile
+// per pair. CTA r loads rows [128 r, 128 r + 128) of the tile's A slice and of
+// its B slice (16 KiB + 16 KiB per stage), so each SM streams a third less
+// from L2 and writes a third less into shared memory than the single-CTA
+// 128 x 256 tile. The even CTA issues the MMAs for both; each CTA's TMEM holds
+// its 128 accumulator rows x 256 columns and its own 4 epilogue warps drain it.
+//   full[s]   (even CTA) : both CTAs' TMA bytes of stage s
+//   empty[s]  (each CTA) : pair MMA commit, multicast to both CTAs
+//   tfull[a]  (each CTA) : pair MMA commit after a tile's last K step
+//   tempty[a] (even CTA) : 256 epilogue arrivals, 128 from each CTA
+constexpr int kPairStages = 6;
+constexpr int kPairAStageBytes = kBM * kBK * 2;         // 16 KiB
+constexpr int kPairBStageBytes = (kBN / 2) * kBK * 2;   // 16 KiB
+constexpr size_t kPairSmemBytes =
+    1024 + static_cast<size_t>(kPairStages) * (kPairAStageBytes + kPairBStageBytes) +
+    kBarrierBytes;
+
+template <class Epi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_persistent_pair(const __grid_constant__ CUtensorMap mapA,
+                         const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
+                         const typename Epi::Args ea, int* dev_err) {
+  constexpr bool kAMN = Epi::kAMN;
+  constexpr bool kBMN = Epi::kBMN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kPairStages * kPairAStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kPairStages * kPairBStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kPairStages;
+  uint64_t* tfull = bars + 2 * kPairStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* done_bar = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * kEpiThreads);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Pair tiles: 256 rows of M (two 128-row halves) x 256 columns of N.
+  GemmGeom pg = g;
+  pg.tiles_m = (g.tiles_m + 1) / 2;
+  const int num_tiles = pg.tiles_m * pg.tiles_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- TMA producer (both CTAs)
+      const uint64_t pol = l2_policy_evict_normal();
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      for (int t = cluster; t < num_tiles; t += nclusters) {
+        int tm2, tn;
+        tile_coords(pg, t, tm2, tn);
+        const int m0 = tm2 * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int n0 = tn * kBN + static_cast<int>(rank) * (kBN / 2);
+        bool ok = true;
+        for (int kb = 0; kb < g.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, dev_err)) {
+            ok = false;
+            break;
+          }
+          if (leader)
+            mbar_arrive_expect_tx(&full[s], 2 * (kPairAStageBytes + kPairBStageBytes));
+          const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
+          uint8_t* a = sA + s * kPairAStageBytes;
+          uint8_t* b = sB + s * kPairBStageBytes;
+          const int k0 = kb * kBK;
+          if constexpr (!kAMN) {
+            tma_load_2d_pair(a, &mapA, fb, k0 + g.a_k_off, m0 + g.a_mn_off, pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j)
+              tma_load_2d_pair(a + j * kMnBoxBytes, &mapA, fb, m0 + g.a_mn_off + j * 64,
+                               k0 + g.a_k_off, pol);
+          }
+          if constexpr (!kBMN) {
+            tma_load_2d_pair(b, &mapB, fb, k0 + g.b_k_off, n0 + g.b_mn_off, pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < (kBN / 2) / 64; ++j)
+              tma_load_2d_pair(b + j * kMnBoxBytes, &mapB, fb, n0 + g.b_mn_off + j * 64,
+                               k0 + g.b_k_off, pol);
+          }
+          ++issued;
+          if (++s == kPairStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: a stage's loads have landed once the pair MMA that read it committed.
+      for (long long i = (issued > kPairStages ? issued - kPairStages : 0); i < issued; ++i)
+        mbar_drain(&empty[i % kPairStages], static_cast<uint32_t>((i / kPairStages) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // ------------------------------------------- MMA issuer (even CTA)
+        constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, kAMN, kBMN);
+        int s = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int t = cluster; t < num_tiles; t += nclusters) {
+          if (!mbar_wait(&tempty[acc], aph ^ 1, abort_flag, dev_err)) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+          bool ok = true;
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            if (!mbar_wait(&full[s], ph, abort_flag, dev_err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + s * kPairAStageBytes);
+            const uint32_t b_addr = smem_u32(sB + s * kPairBStageBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              const uint64_t ad =
+                  kAMN ? smem_desc_sw128(a_addr + kk * (kUmmaK * 128), kMnBoxBytes, 1024)
+                       : smem_desc_sw128(a_addr + kk * (kUmmaK * 2), 16, 1024);
+              const uint64_t bd =
+                  kBMN ? smem_desc_sw128(b_addr + kk * (kUmmaK * 128), kMnBoxBytes, 1024)
+                       : smem_desc_sw128(b_addr + kk * (kUmmaK * 2), 16, 1024);
+              umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            umma_commit_pair(&empty[s], 0x3);
+            if (++s == kPairStages) {
+              s = 0;
+              ph ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair(&tfull[acc], 0x3);
+          acc ^= 1;
+          if (acc == 0) aph ^= 1;
+        }
+        umma_commit_pair(done_bar, 0x3);
+      }
+      // Both CTAs: every pair MMA must finish before TMEM is released.
+      mbar_drain(done_bar, 0);
+    }
+  } else {
+    // ---------------------------------------------------- epilogue (both CTAs)
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int t = cluster; t < num_tiles; t += nclusters) {
+      int tm2, tn;
+      tile_coords(pg, t, tm2, tn);
+      if (!mbar_wait(&tfull[acc], aph, abort_flag, dev_err)) break;
+      tc_fence_after();
+      const uint32_t taddr =
+          tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+      Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr);
+      tc_fence_before();
+      mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      acc ^= 1;
+      if (acc == 0) aph ^= 1;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
 }  // namespace flce
