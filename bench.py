@@ -39,6 +39,12 @@ WORKLOAD = "llama3_head"
 METRIC = "FLCE fwd+bwd ms, tokens/s, TFLOP/s (% bf16 TC peak) @ 8192×4096×128256"
 PAGES_MS = 19.897  # Liger-Kernel commit 95b01e9, B200, same shape (context)
 L2_FLUSH_BYTES = 256 << 20
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of each CTA-pair
+# GEMM from one ncu capture (profiles/gemm_cta_pair_fwd_dw_dx_8192x4096x32768.md):
+# the backward launches there have this workload's per-launch shape (one
+# 16384-column vocabulary block); the forward's is scaled by V (128256/32768).
+# Must be re-measured (or removed) whenever one of these kernels changes.
+TRAFFIC_PER_LAUNCH = {"bwd_dw": 1.466e9, "bwd_dx": 1.373e9, "fwd_lse": 1.342e9 * 128256 / 32768}
 
 
 def peaks():
@@ -101,6 +107,18 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(value: float, ws: int, device) -> float:
+    """Largest value over all ranks (one all-reduce MAX); the identity for a
+    single process. Timing uses it so the slowest replica sets the number."""
+    if ws <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def dist_env():
@@ -201,7 +219,8 @@ def run_ours(args):
                 reduction=wl.reduction)
     N, H, V = wl.N, wl.H, wl.V
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", **opts), dtype=torch.uint8, device=dev)
-    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", **opts), dtype=torch.uint8, device=dev)
+    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", bwd_vocab_block=args.bwd_vocab_block,
+                                            **opts), dtype=torch.uint8, device=dev)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dx = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
@@ -211,11 +230,13 @@ def run_ours(args):
     ftr, btr = F.KernelTrace(8), F.KernelTrace(256)
     host_loss = torch.empty(1, dtype=torch.float32).pin_memory()
 
+    bvb = args.bwd_vocab_block
+
     def step(trace=False):
         F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), trace=ftr if trace else None,
                        **opts)
         F.flce_backward(dloss, lse, x, W, None, y, workspace=bws, out=(dx, dW, None),
-                        trace=btr if trace else None, **opts)
+                        trace=btr if trace else None, bwd_vocab_block=bvb, **opts)
 
     def barrier():
         if ws > 1:
@@ -248,11 +269,36 @@ def run_ours(args):
     wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = sum(step_ms) / len(step_ms)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), ws, dev)
+
+    # ---- stored-probability backward (no logits recompute), same timing rules
+    stored = None
+    if not args.no_stored_mode:
+        saved = torch.empty(F.flce_saved_size(N, H, V, **opts), dtype=torch.uint8, device=dev)
+
+        def step_stored():
+            F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), saved=saved, **opts)
+            F.flce_backward(dloss, lse, x, W, None, y, workspace=bws, out=(dx, dW, None),
+                            saved=saved, bwd_vocab_block=bvb, **opts)
+
+        for _ in range(args.warmup):
+            step_stored()
+        barrier()
+        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            sev[i][0].record(stream)
+            step_stored()
+            sev[i][1].record(stream)
+        barrier()
+        sms = max_over_ranks(sum(a.elapsed_time(b) for a, b in sev) / args.steps, ws, dev)
+        stored = {"ms_per_step": sms, "value": ws * N / (sms * 1e-3), "unit": "tokens/s",
+                  "tflops_6nhv": 6.0 * N * H * V / (sms * 1e-3) / 1e12,
+                  "saved_bytes": saved.numel(),
+                  "note": "flce_forward_store/flce_backward_store: fp16 tile probabilities "
+                          "kept from the forward, no logits recompute (6NHV flops)"}
+        del saved
 
     # ---- end to end through the C ABI with host buffers
     for _ in range(2):
@@ -269,11 +315,7 @@ def run_ours(args):
         host_loss.copy_(loss, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, ws, dev)
 
     # ---- roofline of the dominant kernel
     flops_per = {"fwd_lse": 2.0 * N * H * V, "bwd_dlogits": 2.0 * N * H * V,
@@ -292,7 +334,9 @@ def run_ours(args):
                 "launches_per_step": len(per_kernel[dom]) // steps_,
                 "ms_per_step": dom_ms_per_step,
                 "algorithmic_flops_per_step": flops_per[dom],
-                "traffic": None}
+                "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
+                            and os.environ.get("FLCE_CTA_PAIR", "1") != "0" else None),
+                "traffic_unit": "bytes per launch (ncu dram read + write)"}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm"],
                 "unit": "GB/s", "frac": None, "traffic": None}
@@ -309,7 +353,7 @@ def run_ours(args):
         "config": {"workload": f"{wl.name}: N={N} H={H} V={V} bf16, mean, no bias, dloss=1",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "flushed (256 MiB write) before each timed step, outside the events",
-                   "bwd_vocab_block": 16384, "dW_dtype": "fp32",
+                   "bwd_vocab_block": args.bwd_vocab_block or 16384, "dW_dtype": "fp32",
                    "gemm": "cta pair" if os.environ.get("FLCE_CTA_PAIR", "1") != "0" else "single cta",
                    "N": N, "H": H, "V": V},
         "tflops_8nhv": tflops, "frac_bf16_peak_8nhv": tflops / pk["bf16_sus"],
@@ -323,6 +367,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": 4},
         "clocks": clk,
         "wall_s_timed": wall,
+        "stored_mode": stored,
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
@@ -342,6 +387,9 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="N,H,V override (profiling captures only)")
+    ap.add_argument("--no-stored-mode", action="store_true")
+    ap.add_argument("--bwd-vocab-block", type=int, default=0,
+                    help="backward vocabulary block (multiple of 256); 0 = library default")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -83,6 +83,12 @@ typedef struct {
   int32_t dW_fp32;          /* backward: 1 = dW written as fp32, 0 = bf16 */
   int32_t db_fp32;          /* backward: 1 = db written as fp32, 0 = bf16 */
   int64_t bwd_vocab_block;  /* backward vocab block BVc (multiple of 256); 0 = library default */
+  int64_t vocab_start;      /* shard calls only: first vocabulary id of W's rows */
+  int64_t vocab_total;      /* shard calls only: full vocabulary size (0 = W is the whole
+                               vocabulary; the plain calls require 0 or V) */
+  int32_t input_fp16;       /* 0: x, W, b are bf16; 1: they are fp16 (dx, and dW / db when
+                               not fp32, are then fp16 too) */
+  int32_t reserved;         /* must be 0 */
 } flce_params_t;
 
 /* Kernel kinds reported by the traced entry points. */
@@ -121,6 +127,7 @@ size_t flce_workspace_size(const flce_params_t* p, int which);
  * Writes loss (fp32, [1] for sum/mean, [N] for none) and lse ([N] fp32,
  * natural log, for every token including ignored ones). lse is what
  * flce_backward needs from the forward pass.
+ * (x, W, b are fp16 instead when input_fp16 = 1.)
  * x, W, b and the workspace must be 16-byte aligned. dev_err: one device
  * int32 (may be NULL to skip device error reporting).
  */
@@ -152,6 +159,69 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
                                    void* dx, void* dW, void* db, void* workspace,
                                    size_t workspace_bytes, int32_t* dev_err, void* stream,
                                    flce_trace_t* trace);
+
+/*
+ * Stored-probability mode: no logits recompute in the backward pass.
+ * flce_forward_store computes what flce_forward does and also keeps, in the
+ * caller's `saved` buffer (flce_saved_size(p) bytes, 16-byte aligned), every
+ * logit's probability relative to its 128 x 256 tile's row maximum,
+ * q = exp(z - m_t) in fp16, plus the maxima m_t (fp32). flce_backward_store
+ * then forms dlogits = (1 + 2 lam lse) q exp(m_t - lse) - eps/V - (1 - eps)
+ * delta_y from that state (an HBM pass) instead of recomputing x W^T, saving
+ * 2 N H V flops (a quarter of the step) for 2 N V bytes of memory. `saved`
+ * must be left untouched between the two calls; workspaces are as in the
+ * plain calls (flce_workspace_size). trace may be NULL.
+ */
+size_t flce_saved_size(const flce_params_t* p);
+flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const void* W,
+                                 const void* b, const int64_t* y, float* loss, float* lse,
+                                 void* saved, size_t saved_bytes, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                 flce_trace_t* trace);
+flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss, const float* lse,
+                                  const void* saved, size_t saved_bytes, const void* x,
+                                  const void* W, const void* b, const int64_t* y, void* dx,
+                                  void* dW, void* db, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_err, void* stream, flce_trace_t* trace);
+
+/*
+ * Vocabulary-parallel FLCE (DeepSpeed PR #8792, "What": each rank holds a
+ * [vocab / tp] block of the LM head; forward runs one MAX and one SUM
+ * all-reduce of per-token statistics, backward reduces the hidden gradient
+ * in fp32 before casting). For these calls W (and b) are the rows
+ * [vocab_start, vocab_start + V) of a vocab_total vocabulary (params fields),
+ * shards may be uneven, and y holds global vocabulary ids on every shard.
+ * The collectives themselves are the caller's (NCCL, gloo, or a host loop):
+ *
+ *   1. flce_forward_shard  -> stats [4, N] fp32: rows (m, d, z_y, sum_z) with
+ *      m = max_v z log2(e) over the shard, d = sum_v 2^(z log2(e) - m),
+ *      z_y = the target logit if y is in the shard else 0, sum_z (0 without
+ *      label smoothing). Workspace: flce_workspace_size(p, 0).
+ *   2. caller: M = all-reduce MAX of row 0.
+ *   3. flce_shard_rescale(stats, M): d <- d 2^(m - M), m <- M.
+ *   4. caller: all-reduce SUM of rows 1..3.
+ *   5. flce_loss_from_stats (params with V = vocab_total and vocab_total = 0,
+ *      or the shard's params) -> loss, lse exactly as flce_forward would give
+ *      for the whole vocabulary. Workspace: flce_workspace_size(p, 0).
+ *   6. flce_backward_shard(global lse) -> this shard's dW rows and db, and an
+ *      fp32 partial dx [N, H]; caller: all-reduce SUM of dx_partial, then
+ *      flce_cast_f32 (16-byte aligned src and dst) to the operand type
+ *      (dst_fp16 = input_fp16) for dx.
+ */
+flce_status_t flce_forward_shard(const flce_params_t* p, const void* x, const void* W,
+                                 const void* b, const int64_t* y, float* stats, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream);
+flce_status_t flce_shard_rescale(const flce_params_t* p, float* stats, const float* global_max,
+                                 void* stream);
+flce_status_t flce_loss_from_stats(const flce_params_t* p, const float* stats, const int64_t* y,
+                                   float* loss, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, void* stream);
+flce_status_t flce_backward_shard(const flce_params_t* p, const float* dloss, const float* lse,
+                                  const void* x, const void* W, const void* b, const int64_t* y,
+                                  float* dx_partial, void* dW, void* db, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_err, void* stream);
+flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_fp16,
+                            void* stream);
 
 /*
  * Forward without a workspace argument, for callers that cannot allocate

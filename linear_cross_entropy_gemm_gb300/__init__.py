@@ -26,7 +26,7 @@ from ._lib import FlceError, params
 __all__ = [
     "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
     "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
-    "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace",
+    "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace", "flce_saved_size",
 ]
 
 _err_words = {}
@@ -53,13 +53,16 @@ def device_error_word(device) -> torch.Tensor:
     return w
 
 
+_OPERAND_DTYPES = (torch.bfloat16, torch.float16)
+
+
 def _check_inputs(x, W, b, y):
     if not (x.is_cuda and W.is_cuda and y.is_cuda):
         raise ValueError("flce: x, W and y must be CUDA tensors")
-    if x.dtype != torch.bfloat16 or W.dtype != torch.bfloat16:
-        raise TypeError("flce: x and W must be bf16")
-    if b is not None and (b.dtype != torch.bfloat16 or not b.is_cuda):
-        raise TypeError("flce: b must be a bf16 CUDA tensor")
+    if x.dtype not in _OPERAND_DTYPES or W.dtype != x.dtype:
+        raise TypeError("flce: x and W must both be bf16 or both fp16")
+    if b is not None and (b.dtype != x.dtype or not b.is_cuda):
+        raise TypeError("flce: b must be a CUDA tensor of x's dtype")
     if y.dtype != torch.int64:
         raise TypeError("flce: y must be int64")
     if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[1] or y.shape != (x.shape[0],):
@@ -99,21 +102,31 @@ def flce_workspace_size(N, H, V, which: str, **opts) -> int:
     return int(_lib.load().flce_workspace_size(p, 0 if which == "forward" else 1))
 
 
+def flce_saved_size(N, H, V, **opts) -> int:
+    """Bytes of the state flce_forward(..., saved=) keeps for the stored-
+    probability backward (fp16 tile probabilities + tile maxima, ~2 N V bytes)."""
+    return int(_lib.load().flce_saved_size(params(N, H, V, **opts)))
+
+
 def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: torch.Tensor, *,
                  ignore_index: int = -100, label_smoothing: float = 0.0,
                  lse_square_scale: float = 0.0, logit_scale: float = 1.0,
                  reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
                  out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
-                 stream=None, trace: Optional[KernelTrace] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 stream=None, trace: Optional[KernelTrace] = None,
+                 saved: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss and per-token lse. loss is a 0-dim fp32 tensor (sum/mean) or [N]
-    fp32 (none); lse is [N] fp32. Runs on the current stream, no sync."""
+    fp32 (none); lse is [N] fp32. Runs on the current stream, no sync.
+    With ``saved`` (a uint8 CUDA tensor of flce_saved_size bytes) the forward
+    also keeps the state the stored-probability backward needs."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
     V = W.shape[0]
     p = params(N, H, V, ignore_index=ignore_index, label_smoothing=label_smoothing,
                lse_square_scale=lse_square_scale, logit_scale=logit_scale,
-               reduction=reduction, has_bias=b is not None)
+               reduction=reduction, has_bias=b is not None,
+               input_fp16=x.dtype == torch.float16)
     dev = x.device
     if out is not None:
         loss, lse = out
@@ -123,9 +136,16 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     need = lib.flce_workspace_size(p, 0)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    args = (p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse), _ptr(workspace),
-            workspace.numel(), _ptr(device_error_word(dev)), _stream(stream))
-    st = lib.flce_forward(*args) if trace is None else lib.flce_forward_traced(*args, trace.struct)
+    if saved is not None:
+        _check_saved(saved, lib, p)
+        st = lib.flce_forward_store(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse),
+                                    _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
+                                    _ptr(device_error_word(dev)), _stream(stream),
+                                    None if trace is None else trace.struct)
+    else:
+        args = (p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse), _ptr(workspace),
+                workspace.numel(), _ptr(device_error_word(dev)), _stream(stream))
+        st = lib.flce_forward(*args) if trace is None else lib.flce_forward_traced(*args, trace.struct)
     if st != _lib.FLCE_OK:
         raise FlceError(st, "flce_forward")
     return (loss if reduction == "none" else loss.view(())), lse
@@ -137,8 +157,11 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                   logit_scale: float = 1.0, reduction: str = "mean",
                   dW_dtype: torch.dtype = torch.float32, db_dtype: torch.dtype = torch.float32,
                   bwd_vocab_block: int = 0, workspace: Optional[torch.Tensor] = None,
-                  out: Optional[Tuple] = None, stream=None, trace: Optional[KernelTrace] = None):
-    """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None."""
+                  out: Optional[Tuple] = None, stream=None, trace: Optional[KernelTrace] = None,
+                  saved: Optional[torch.Tensor] = None):
+    """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None.
+    With ``saved`` (filled by flce_forward(..., saved=)) the logits are not
+    recomputed: dlogits come from the stored tile probabilities."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
@@ -151,29 +174,44 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
         raise ValueError("flce: dloss must have N elements (none) or 1 (sum/mean)")
     if lse.dtype != torch.float32 or lse.shape != (N,):
         raise ValueError("flce: lse must be the forward's [N] fp32 output")
-    if dW_dtype not in (torch.float32, torch.bfloat16) or db_dtype not in (torch.float32, torch.bfloat16):
-        raise TypeError("flce: dW_dtype and db_dtype must be fp32 or bf16")
+    if dW_dtype not in (torch.float32, x.dtype) or db_dtype not in (torch.float32, x.dtype):
+        raise TypeError("flce: dW_dtype and db_dtype must be fp32 or x's dtype")
     p = params(N, H, V, ignore_index=ignore_index, label_smoothing=label_smoothing,
                lse_square_scale=lse_square_scale, logit_scale=logit_scale,
                reduction=reduction, has_bias=b is not None,
                dW_fp32=dW_dtype == torch.float32, db_fp32=db_dtype == torch.float32,
-               bwd_vocab_block=bwd_vocab_block)
+               bwd_vocab_block=bwd_vocab_block, input_fp16=x.dtype == torch.float16)
     if out is not None:
         dx, dW, db = out
     else:
-        dx = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(N, H, dtype=x.dtype, device=dev)
         dW = torch.empty(V, H, dtype=dW_dtype, device=dev)
         db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
     need = lib.flce_workspace_size(p, 1)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    args = (p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW),
-            _ptr(db), _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
-            _stream(stream))
-    st = lib.flce_backward(*args) if trace is None else lib.flce_backward_traced(*args, trace.struct)
+    if saved is not None:
+        _check_saved(saved, lib, p)
+        st = lib.flce_backward_store(p, _ptr(dloss), _ptr(lse), _ptr(saved), saved.numel(), _ptr(x),
+                                     _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW), _ptr(db),
+                                     _ptr(workspace), workspace.numel(),
+                                     _ptr(device_error_word(dev)), _stream(stream),
+                                     None if trace is None else trace.struct)
+    else:
+        args = (p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW),
+                _ptr(db), _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
+                _stream(stream))
+        st = lib.flce_backward(*args) if trace is None else lib.flce_backward_traced(*args, trace.struct)
     if st != _lib.FLCE_OK:
         raise FlceError(st, "flce_backward")
     return dx, dW, db
+
+
+def _check_saved(saved, lib, p):
+    if saved.dtype != torch.uint8 or not saved.is_cuda or not saved.is_contiguous():
+        raise TypeError("flce: saved must be a contiguous uint8 CUDA tensor")
+    if saved.numel() < lib.flce_saved_size(p):
+        raise ValueError("flce: saved is smaller than flce_saved_size()")
 
 
 def flce_read_device_error(device=None, stream=None) -> int:
@@ -194,11 +232,18 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, x, target, weight, bias=None, ignore_index=-100, label_smoothing=0.0,
-                lse_square_scale=0.0, logit_scale=1.0, reduction="mean"):
+                lse_square_scale=0.0, logit_scale=1.0, reduction="mean", recompute=True):
+        saved = None
+        if not recompute:
+            n = flce_saved_size(x.shape[0], x.shape[1], weight.shape[0],
+                                label_smoothing=label_smoothing,
+                                input_fp16=x.dtype == torch.float16)
+            saved = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
         loss, lse = flce_forward(x, weight, bias, target, ignore_index=ignore_index,
                                  label_smoothing=label_smoothing,
                                  lse_square_scale=lse_square_scale, logit_scale=logit_scale,
-                                 reduction=reduction)
+                                 reduction=reduction, saved=saved)
+        ctx.saved_state = saved
         ctx.save_for_backward(x, target, weight, bias, lse)
         ctx.opts = dict(ignore_index=ignore_index, label_smoothing=label_smoothing,
                         lse_square_scale=lse_square_scale, logit_scale=logit_scale,
@@ -209,26 +254,30 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
     def backward(ctx, dloss):
         x, target, weight, bias, lse = ctx.saved_tensors
         dx, dW, db = flce_backward(dloss.float().contiguous(), lse, x, weight, bias, target,
-                                   dW_dtype=torch.float32, db_dtype=torch.float32, **ctx.opts)
+                                   dW_dtype=torch.float32, db_dtype=torch.float32,
+                                   saved=ctx.saved_state, **ctx.opts)
+        ctx.saved_state = None
         dW = dW.to(weight.dtype)
         db = None if db is None else db.to(bias.dtype)
-        return dx, None, dW, db, None, None, None, None, None
+        return dx, None, dW, db, None, None, None, None, None, None
 
 
 def fused_linear_cross_entropy(x, target, weight, bias=None, ignore_index=-100,
                                label_smoothing=0.0, lse_square_scale=0.0, logit_scale=1.0,
-                               reduction="mean"):
-    """Functional form; x [N, H] bf16, target [N] int64, weight [V, H] bf16."""
+                               reduction="mean", recompute=True):
+    """Functional form; x [N, H] bf16, target [N] int64, weight [V, H] bf16.
+    recompute=False keeps fp16 tile probabilities (~2 N V bytes) from the
+    forward so the backward skips the logits GEMM."""
     return FusedLinearCrossEntropyFunction.apply(x, target, weight, bias, ignore_index,
                                                  label_smoothing, lse_square_scale,
-                                                 logit_scale, reduction)
+                                                 logit_scale, reduction, recompute)
 
 
 class FusedLinearCrossEntropyLoss(torch.nn.Module):
     """Module form: flattens x [..., H] and target [...] to [N, H] and [N]."""
 
     def __init__(self, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
-                 logit_scale=1.0, reduction="mean"):
+                 logit_scale=1.0, reduction="mean", recompute=True):
         super().__init__()
         if reduction not in ("none", "sum", "mean"):
             raise ValueError(f"reduction: {reduction} is not supported")
@@ -237,9 +286,10 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         self.lse_square_scale = lse_square_scale
         self.logit_scale = logit_scale
         self.reduction = reduction
+        self.recompute = recompute
 
     def forward(self, x, target, weight, bias=None):
         return fused_linear_cross_entropy(
             x.reshape(-1, x.shape[-1]).contiguous(), target.reshape(-1).contiguous(), weight,
             bias, self.ignore_index, self.label_smoothing, self.lse_square_scale,
-            self.logit_scale, self.reduction)
+            self.logit_scale, self.reduction, self.recompute)

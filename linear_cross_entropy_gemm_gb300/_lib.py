@@ -37,6 +37,10 @@ class FlceParams(ctypes.Structure):
         ("dW_fp32", ctypes.c_int32),
         ("db_fp32", ctypes.c_int32),
         ("bwd_vocab_block", ctypes.c_int64),
+        ("vocab_start", ctypes.c_int64),
+        ("vocab_total", ctypes.c_int64),
+        ("input_fp16", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -87,6 +91,23 @@ def load() -> ctypes.CDLL:
     lib.flce_forward_traced.restype = ctypes.c_int
     lib.flce_backward_traced.argtypes = lib.flce_backward.argtypes + [T]
     lib.flce_backward_traced.restype = ctypes.c_int
+    lib.flce_saved_size.argtypes = [P]
+    lib.flce_saved_size.restype = sz
+    lib.flce_forward_store.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp, vp, T]
+    lib.flce_forward_store.restype = ctypes.c_int
+    lib.flce_backward_store.argtypes = [P, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                        vp, vp, T]
+    lib.flce_backward_store.restype = ctypes.c_int
+    lib.flce_forward_shard.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.flce_forward_shard.restype = ctypes.c_int
+    lib.flce_shard_rescale.argtypes = [P, vp, vp, vp]
+    lib.flce_shard_rescale.restype = ctypes.c_int
+    lib.flce_loss_from_stats.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.flce_loss_from_stats.restype = ctypes.c_int
+    lib.flce_backward_shard.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+    lib.flce_backward_shard.restype = ctypes.c_int
+    lib.flce_cast_f32.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int32, vp]
+    lib.flce_cast_f32.restype = ctypes.c_int
     lib.flce_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.flce_read_device_error.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]
@@ -99,10 +120,11 @@ def load() -> ctypes.CDLL:
 
 def params(N, H, V, *, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
            logit_scale=1.0, reduction="mean", has_bias=False, dW_fp32=True, db_fp32=True,
-           bwd_vocab_block=0) -> FlceParams:
+           bwd_vocab_block=0, vocab_start=0, vocab_total=0, input_fp16=False) -> FlceParams:
     if reduction not in REDUCTION:
         raise ValueError(f"reduction must be one of {sorted(REDUCTION)}, got {reduction!r}")
     return FlceParams(int(N), int(H), int(V), int(ignore_index), float(label_smoothing),
                       float(lse_square_scale), float(logit_scale), REDUCTION[reduction],
                       int(bool(has_bias)), int(bool(dW_fp32)), int(bool(db_fp32)),
-                      int(bwd_vocab_block))
+                      int(bwd_vocab_block), int(vocab_start), int(vocab_total),
+                      int(bool(input_fp16)), 0)

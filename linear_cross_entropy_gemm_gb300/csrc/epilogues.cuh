@@ -9,6 +9,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "gemm_engine.cuh"
 
@@ -16,10 +17,11 @@ namespace flce {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Bias of 32 consecutive vocab columns starting at col0 (< V); zero past V.
+// Bias (bf16 or fp16 bits) of 32 consecutive vocab columns starting at
+// col0 (< V); zero past V.
 template <bool HAS_BIAS>
-__device__ __forceinline__ void load_bias32(const __nv_bfloat16* __restrict__ bias, int col0, int V,
-                                            float (&bv)[32]) {
+__device__ __forceinline__ void load_bias32(const uint16_t* __restrict__ bias, int col0, int V,
+                                            float (&bv)[32], bool fp16) {
   if constexpr (!HAS_BIAS) {
 #pragma unroll
     for (int j = 0; j < 32; ++j) bv[j] = 0.f;
@@ -32,15 +34,34 @@ __device__ __forceinline__ void load_bias32(const __nv_bfloat16* __restrict__ bi
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          bv[q * 8 + 2 * e] = __uint_as_float(w[e] << 16);
-          bv[q * 8 + 2 * e + 1] = __uint_as_float(w[e] & 0xFFFF0000u);
+          bv[q * 8 + 2 * e] = unpack_16(w[e] & 0xFFFFu, fp16);
+          bv[q * 8 + 2 * e + 1] = unpack_16(w[e] >> 16, fp16);
         }
       }
     } else {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) bv[j] = (col0 + j < V) ? __bfloat162float(bias[col0 + j]) : 0.f;
+      for (int j = 0; j < 32; ++j)
+        bv[j] = (col0 + j < V) ? unpack_16(__ldg(bias + col0 + j), fp16) : 0.f;
     }
   }
+}
+
+// 32 fp32 values -> 64 bytes of the 16-bit operand type at dst (16-B aligned).
+__device__ __forceinline__ void store32_16(void* dst, const float (&v)[32], bool fp16) {
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_16x2(v[q * 8 + 0], v[q * 8 + 1], fp16);
+    u.y = pack_16x2(v[q * 8 + 2], v[q * 8 + 3], fp16);
+    u.z = pack_16x2(v[q * 8 + 4], v[q * 8 + 5], fp16);
+    u.w = pack_16x2(v[q * 8 + 6], v[q * 8 + 7], fp16);
+    o[q] = u;
+  }
+}
+
+__device__ __forceinline__ uint16_t to16(float f, bool fp16) {
+  return static_cast<uint16_t>(pack_16x2(f, 0.f, fp16) & 0xFFFFu);
 }
 
 // Column sums of a 32 x 32 block held one row per lane: afterwards lane L
@@ -64,8 +85,10 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
 // partials (m = max z log2e, d = sum 2^(z log2e - m)), the tile's sum of z
 // (label smoothing only) and the target logit z_y when y falls in the tile.
 struct FwdLseArgs {
-  const __nv_bfloat16* bias;
+  const uint16_t* bias;  // bf16 or fp16 bits
+  int fp16;
   const int64_t* y;
+  int64_t y_off;  // vocabulary id of W's first row (vocabulary shards; else 0)
   float scale;
   int V;
   int Ntok;
@@ -83,7 +106,7 @@ struct FwdLseEpi {
                               int, int, uint32_t taddr) {
     const int row = tm * kBM + row_in_tile;
     const int v0 = tn * kBN;
-    const int64_t yv = row < a.Ntok ? __ldg(a.y + row) : -1;
+    const int64_t yv = row < a.Ntok ? __ldg(a.y + row) - a.y_off : -1;
     const int ty = (yv >= v0 && yv < static_cast<int64_t>(v0) + kBN) ? static_cast<int>(yv - v0) : -1;
     float m = -INFINITY, d = 0.f, S = 0.f, zt = 0.f;
 #pragma unroll 1
@@ -91,7 +114,7 @@ struct FwdLseEpi {
       float v[32], bv[32];
       tmem_ld_32cols(taddr + c * 32, v);
       const int col0 = v0 + c * 32;
-      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv);
+      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
       float cm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -121,6 +144,85 @@ struct FwdLseEpi {
   }
 };
 
+// --------------------------------------------- forward, keeping probabilities
+// As FwdLseEpi, and also writes q = 2^(z log2e - m_t) for every logit of the
+// tile as fp16 into probs[row, v] (m_t = the tile's row max, written to
+// part_m), so a later backward can form dL = a_n q 2^(m_t - lse2) - c_n - t_n [v == y]
+// without recomputing the logits. Two passes over the accumulator: the first
+// finds m_t (and z_y, sum z), the second exponentiates, sums and stores.
+struct FwdStoreArgs {
+  FwdLseArgs base;
+  __half* probs;  // [Ntok, ld_p]
+  int ld_p;       // tiles_v * 256
+};
+
+template <bool HAS_BIAS, bool HAS_SMOOTH>
+struct FwdStoreEpi {
+  static constexpr bool kAMN = false, kBMN = false;
+  using Args = FwdStoreArgs;
+  __device__ static void tile(const Args& A, const GemmGeom&, int tm, int tn, int row_in_tile,
+                              int, int, uint32_t taddr) {
+    const FwdLseArgs& a = A.base;
+    const int row = tm * kBM + row_in_tile;
+    const int v0 = tn * kBN;
+    const int64_t yv = row < a.Ntok ? __ldg(a.y + row) - a.y_off : -1;
+    const int ty = (yv >= v0 && yv < static_cast<int64_t>(v0) + kBN) ? static_cast<int>(yv - v0) : -1;
+    float m = -INFINITY, S = 0.f, zt = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32], bv[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int col0 = v0 + c * 32;
+      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float z = (v[j] + bv[j]) * a.scale;
+        const bool ok = col0 + j < a.V;
+        if constexpr (HAS_SMOOTH) S += ok ? z : 0.f;
+        zt = (c * 32 + j == ty) ? z : zt;
+        m = ok ? fmaxf(m, z * kLog2e) : m;
+      }
+    }
+    float d = 0.f;
+    __half* prow = A.probs + static_cast<size_t>(row < a.Ntok ? row : 0) * A.ld_p + v0;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32], bv[32];
+      tmem_ld_32cols(taddr + c * 32, v);
+      const int col0 = v0 + c * 32;
+      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float z = (v[j] + bv[j]) * a.scale;
+        const float q = (col0 + j < a.V) ? fast_exp2(fmaf(z, kLog2e, -m)) : 0.f;
+        d += q;
+        v[j] = q;
+      }
+      if (row < a.Ntok) {
+        uint4* dst = reinterpret_cast<uint4*>(prow + c * 32);
+#pragma unroll
+        for (int qd = 0; qd < 4; ++qd) {
+          uint4 u;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __half2 h = __floats2half2_rn(v[qd * 8 + 2 * e], v[qd * 8 + 2 * e + 1]);
+            w[e] = *reinterpret_cast<const uint32_t*>(&h);
+          }
+          dst[qd] = u;
+        }
+      }
+    }
+    if (row < a.Ntok) {
+      const size_t o = static_cast<size_t>(tn) * a.Ntok + row;
+      a.part_m[o] = m;
+      a.part_d[o] = d;
+      if constexpr (HAS_SMOOTH) a.part_s[o] = S;
+      if (ty >= 0) a.zy[row] = zt;
+    }
+  }
+};
+
 // ------------------------------------------------- backward: recompute + dL
 // Recomputes a logits tile of the current vocab block, forms
 // dL = a_n p - c_n - t_n [v == y_n] with per-row coefficients
@@ -128,15 +230,18 @@ struct FwdLseEpi {
 // writes it as bf16 into the staged block dL[Ntok, ld] and, with a bias,
 // writes per-warp column sums (fp32, before rounding) for db.
 struct DlogitsArgs {
-  const __nv_bfloat16* bias;
+  const uint16_t* bias;  // bf16 or fp16 bits
+  int fp16;              // dL written as fp16 (else bf16), like the operands
+  const float* dl_scale; // [0]: power-of-two factor applied to dL before rounding
   const int64_t* y;
+  int64_t y_off;       // vocabulary id of W's first row (vocabulary shards; else 0)
   const float4* coef;  // [Ntok]: (lse2, a, c, t)
   float scale;
   int V;
   int Ntok;
   int v0;              // first vocab id of the block
   int Vb;              // vocab ids in the block
-  __nv_bfloat16* dL;   // [Ntok, ld_dL], block-relative columns
+  uint16_t* dL;        // [Ntok, ld_dL], block-relative columns
   int ld_dL;
   float* db_part;      // [tiles_m * 4, ld_db] or null
   int ld_db;
@@ -153,7 +258,8 @@ struct DlogitsEpi {
     const int vt0 = tn * kBN;  // block-relative
     const int vg0 = a.v0 + vt0;
     const float4 cf = row_ok ? __ldg(a.coef + row) : make_float4(0.f, 0.f, 0.f, 0.f);
-    const int64_t yv = row_ok ? __ldg(a.y + row) : -1;
+    const float dls = __ldg(a.dl_scale);
+    const int64_t yv = row_ok ? __ldg(a.y + row) - a.y_off : -1;
     const int ty = (yv >= vg0 && yv < static_cast<int64_t>(vg0) + kBN) ? static_cast<int>(yv - vg0) : -1;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
@@ -161,7 +267,7 @@ struct DlogitsEpi {
       tmem_ld_32cols(taddr + c * 32, v);
       const int colb0 = vt0 + c * 32;
       const int colg0 = vg0 + c * 32;
-      load_bias32<HAS_BIAS>(a.bias, colg0 < a.V ? colg0 : 0, a.V, bv);
+      load_bias32<HAS_BIAS>(a.bias, colg0 < a.V ? colg0 : 0, a.V, bv, a.fp16 != 0);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float z = (v[j] + bv[j]) * a.scale;
@@ -171,16 +277,10 @@ struct DlogitsEpi {
         v[j] = (row_ok && colb0 + j < a.Vb) ? dl : 0.f;
       }
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(a.dL + static_cast<size_t>(row) * a.ld_dL + colb0);
+        float sv[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-          u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-          u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-          u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-          dst[q] = u;
-        }
+        for (int j = 0; j < 32; ++j) sv[j] = v[j] * dls;
+        store32_16(a.dL + static_cast<size_t>(row) * a.ld_dL + colb0, sv, a.fp16 != 0);
       }
       if constexpr (HAS_BIAS) {
         const float colsum = warp_column_sums(v, lane);
@@ -194,8 +294,10 @@ struct DlogitsEpi {
 // ---------------------------------------------------------- backward: dW
 // dW[v0 + r, :] = sum_n dL[n, r] x[n, :] for block-relative vocab row r.
 struct DwArgs {
-  void* out;      // dW [V, ld] fp32 or bf16
-  int out_bf16;
+  void* out;      // dW [V, ld] fp32, or the 16-bit operand type
+  int out_bf16;   // 1: write the 16-bit type (bf16, or fp16 when fp16)
+  int fp16;
+  const float* acc_scale;  // [0]: undoes the dL scale (power of two)
   int ld;         // H
   int row0;       // v0
   int Mrows;      // Vb
@@ -210,10 +312,13 @@ struct DwEpi {
     const int r = tm * kBM + row_in_tile;
     const bool row_ok = r < a.Mrows;
     const size_t orow = static_cast<size_t>(a.row0 + (row_ok ? r : 0)) * a.ld;
+    const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= sc;
       const int col0 = tn * kBN + c * 32;
       if (row_ok && col0 < a.Ncols) store_dw(a, orow, col0, v);
     }
@@ -222,21 +327,13 @@ struct DwEpi {
                                                  const float (&v)[32]) {
     {
       if (a.out_bf16) {
-        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(a.out) + orow + col0;
+        uint16_t* o = reinterpret_cast<uint16_t*>(a.out) + orow + col0;
         if (col0 + 32 <= a.Ncols) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-            u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-            u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-            u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-            reinterpret_cast<uint4*>(o)[q] = u;
-          }
+          store32_16(o, v, a.fp16 != 0);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < a.Ncols - col0) o[j] = __float2bfloat16_rn(v[j]);
+            if (j < a.Ncols - col0) o[j] = to16(v[j], a.fp16 != 0);
         }
       } else {
         float* o = reinterpret_cast<float*>(a.out) + orow + col0;
@@ -260,7 +357,10 @@ struct DwEpi {
 // fp32 buffer; the first block stores, the last one writes bf16 dx.
 struct DxArgs {
   float* acc;             // [Ntok, ld] fp32 (unused when first && last)
-  __nv_bfloat16* out;     // dx [Ntok, ld] bf16
+  uint16_t* out;          // dx [Ntok, ld] bf16 / fp16 (fp32 when out_f32)
+  int fp16;
+  const float* acc_scale; // [0]: undoes the dL scale (power of two)
+  int out_f32;            // last block writes fp32 (vocabulary-shard partial dx)
   int ld;                 // H
   int Ntok;
   int Ncols;              // H
@@ -276,10 +376,13 @@ struct DxEpi {
     const int row = tm * kBM + row_in_tile;
     const bool row_ok = row < a.Ntok;
     const size_t orow = static_cast<size_t>(row_ok ? row : 0) * a.ld;
+    const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] *= sc;
       const int col0 = tn * kBN + c * 32;
       if (row_ok && col0 < a.Ncols) accumulate(a, orow, col0, v);
     }
@@ -300,17 +403,14 @@ struct DxEpi {
             v[4 * q + 3] += p.w;
           }
         }
-        if (a.last) {
-          uint4* o = reinterpret_cast<uint4*>(a.out + orow + col0);
+        if (a.last && a.out_f32) {
+          float* o = reinterpret_cast<float*>(a.out) + orow + col0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]);
-            u.y = pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]);
-            u.z = pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]);
-            u.w = pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]);
-            o[q] = u;
-          }
+          for (int q = 0; q < 8; ++q)
+            reinterpret_cast<float4*>(o)[q] =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else if (a.last) {
+          store32_16(a.out + orow + col0, v, a.fp16 != 0);
         } else {
 #pragma unroll
           for (int q = 0; q < 8; ++q)
@@ -322,8 +422,10 @@ struct DxEpi {
         for (int j = 0; j < 32; ++j) {
           if (j < ncol) {
             const float val = v[j] + (a.first ? 0.f : accp[j]);
-            if (a.last)
-              a.out[orow + col0 + j] = __float2bfloat16_rn(val);
+            if (a.last && a.out_f32)
+              reinterpret_cast<float*>(a.out)[orow + col0 + j] = val;
+            else if (a.last)
+              a.out[orow + col0 + j] = to16(val, a.fp16 != 0);
             else
               accp[j] = val;
           }

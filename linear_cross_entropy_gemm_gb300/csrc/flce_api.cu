@@ -48,17 +48,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// 2-D bf16 tensor [outer, inner] with row pitch `pitch_bytes`, 128-B swizzled
-// boxes of box_inner x box_outer elements; out-of-range elements read as 0.
+// 2-D 16-bit tensor [outer, inner] (bf16, or fp16 when fp16) with row pitch
+// `pitch_bytes`, 128-B swizzled boxes of box_inner x box_outer elements;
+// out-of-range elements read as 0.
 bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-               uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+               uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, bool fp16) {
   auto fn = encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  return fn(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -95,13 +97,31 @@ flce_status_t check_params(const flce_params_t* p) {
   if (p->N < 0 || p->H <= 0 || p->V <= 0) return FLCE_ERR_INVALID_ARG;
   if (p->H % 8 != 0) return FLCE_ERR_ALIGNMENT;  // 16-byte TMA row pitch
   if (p->N > (1LL << 30) || p->V > (1LL << 30) || p->H > (1LL << 20)) return FLCE_ERR_UNSUPPORTED;
+  // Tile indices are int32 in the kernels: the 128 x 256 tile grid of x W^T
+  // (and of the backward GEMMs, which are smaller) must stay below 2^31.
+  if (((p->N + 127) / 128) * ((p->V + 255) / 256) >= (1LL << 31)) return FLCE_ERR_UNSUPPORTED;
   if (p->reduction < 0 || p->reduction > 2) return FLCE_ERR_INVALID_ARG;
   if (!(p->label_smoothing >= 0.f && p->label_smoothing <= 1.f)) return FLCE_ERR_INVALID_ARG;
   if (!(p->lse_square_scale >= 0.f) || !(p->lse_square_scale < INFINITY)) return FLCE_ERR_INVALID_ARG;
   if (!(p->logit_scale > -INFINITY && p->logit_scale < INFINITY)) return FLCE_ERR_INVALID_ARG;
   if (p->bwd_vocab_block < 0 || p->bwd_vocab_block % 256 != 0) return FLCE_ERR_INVALID_ARG;
   if (p->has_bias != 0 && p->has_bias != 1) return FLCE_ERR_INVALID_ARG;
+  if ((p->input_fp16 != 0 && p->input_fp16 != 1) || p->reserved != 0) return FLCE_ERR_INVALID_ARG;
+  if (p->vocab_total == 0) {
+    if (p->vocab_start != 0) return FLCE_ERR_INVALID_ARG;
+  } else if (p->vocab_total < 0 || p->vocab_total > (1LL << 30) || p->vocab_start < 0 ||
+             p->vocab_start + p->V > p->vocab_total) {
+    return FLCE_ERR_INVALID_ARG;
+  }
   return FLCE_OK;
+}
+
+// Full vocabulary size (the shard's own V when unsharded).
+int64_t vocab_total(const flce_params_t* p) { return p->vocab_total > 0 ? p->vocab_total : p->V; }
+
+// Plain (whole-vocabulary) calls: W must hold every vocabulary row.
+bool whole_vocab(const flce_params_t* p) {
+  return p->vocab_total == 0 || (p->vocab_total == p->V && p->vocab_start == 0);
 }
 
 struct Carver {
@@ -148,9 +168,10 @@ int64_t vocab_block(const flce_params_t* p) {
 
 struct BwdWs {
   float4* coef;
-  __nv_bfloat16* dL;
+  uint16_t* dL;      // bf16 or fp16, like the operands
   float* dx_acc;
   float* db_part;
+  float* dl_scale;   // [2]
 };
 
 size_t carve_bwd(const flce_params_t* p, void* base, BwdWs* w) {
@@ -159,15 +180,35 @@ size_t carve_bwd(const flce_params_t* p, void* base, BwdWs* w) {
   const int nblk = cdiv(p->V, bv);
   Carver c(base, 0);
   w->coef = c.take<float4>(N);
-  w->dL = c.take<__nv_bfloat16>(N * static_cast<size_t>(bv));
+  w->dl_scale = c.take<float>(2);
+  w->dL = c.take<uint16_t>(N * static_cast<size_t>(bv));
   w->dx_acc = nblk > 1 ? c.take<float>(N * static_cast<size_t>(p->H)) : nullptr;
   w->db_part = p->has_bias ? c.take<float>(static_cast<size_t>(cdiv(p->N, kBM)) * 4 * bv) : nullptr;
   return c.used() + kAlign;
 }
 
-GemmGeom geom(int M, int N, int K) {
+// State kept between flce_forward_store and flce_backward_store:
+// q [N, tiles_v * 256] fp16, then the tile maxima m_t [tiles_v, N] fp32.
+struct Saved {
+  __half* probs;
+  int ld_p;
+  float* part_m;
+};
+
+size_t carve_saved(const flce_params_t* p, void* base, Saved* sv) {
+  const size_t N = static_cast<size_t>(p->N);
+  const size_t NT = static_cast<size_t>(cdiv(p->V, kBN));
+  Carver c(base, 0);
+  sv->ld_p = static_cast<int>(NT * kBN);
+  sv->probs = c.take<__half>(N * NT * kBN);
+  sv->part_m = c.take<float>(NT * N);
+  return c.used() + kAlign;
+}
+
+GemmGeom geom(int M, int N, int K, bool fp16) {
   GemmGeom g;
   std::memset(&g, 0, sizeof(g));
+  g.ab_fp16 = fp16 ? 1 : 0;
   g.M = M;
   g.N = N;
   g.K = K;
@@ -207,6 +248,18 @@ struct Tracer {
 
 }  // namespace
 
+static flce_status_t forward_impl(const flce_params_t* p, const void* x, const void* W,
+                                  const void* b, const int64_t* y, float* loss, float* lse,
+                                  void* saved, size_t saved_bytes, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                  flce_trace_t* trace, float* shard_stats = nullptr);
+static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, const float* lse,
+                                   const void* saved, size_t saved_bytes, const void* x,
+                                   const void* W, const void* b, const int64_t* y, void* dx,
+                                   void* dW, void* db, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_err, void* stream, flce_trace_t* trace,
+                                   bool shard = false);
+
 extern "C" {
 
 size_t flce_workspace_size(const flce_params_t* p, int which) {
@@ -233,9 +286,41 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
                                   const void* b, const int64_t* y, float* loss, float* lse,
                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                   void* stream, flce_trace_t* trace) {
+  return forward_impl(p, x, W, b, y, loss, lse, nullptr, 0, workspace, workspace_bytes, dev_err,
+                      stream, trace);
+}
+
+flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const void* W,
+                                 const void* b, const int64_t* y, float* loss, float* lse,
+                                 void* saved, size_t saved_bytes, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                 flce_trace_t* trace) {
+  if (!saved && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return forward_impl(p, x, W, b, y, loss, lse, saved, saved_bytes, workspace, workspace_bytes,
+                      dev_err, stream, trace);
+}
+
+size_t flce_saved_size(const flce_params_t* p) {
+  if (check_params(p) != FLCE_OK || p->N == 0) return 0;
+  Saved sv;
+  return carve_saved(p, nullptr, &sv);
+}
+
+}  // extern "C"
+
+static flce_status_t forward_impl(const flce_params_t* p, const void* x, const void* W,
+                                  const void* b, const int64_t* y, float* loss, float* lse,
+                                  void* saved, size_t saved_bytes, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                  flce_trace_t* trace, float* shard_stats) {
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
-  if (!loss) return FLCE_ERR_INVALID_ARG;
+  if (shard_stats) {
+    if (p->vocab_total == 0) return FLCE_ERR_INVALID_ARG;
+    if (p->N == 0) return FLCE_OK;
+  } else if (!whole_vocab(p) || !loss) {
+    return FLCE_ERR_INVALID_ARG;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (p->N == 0) {
     if (p->reduction != FLCE_REDUCTION_NONE &&
@@ -243,28 +328,42 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
       return FLCE_ERR_CUDA;
     return FLCE_OK;
   }
-  if (!x || !W || !y || !lse || !workspace || (p->has_bias && !b)) return FLCE_ERR_INVALID_ARG;
+  if (!x || !W || !y || (!shard_stats && !lse) || !workspace || (p->has_bias && !b))
+    return FLCE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(W) || (p->has_bias && !aligned16(b))) return FLCE_ERR_ALIGNMENT;
   FwdWs w;
   const size_t need = carve_fwd(p, nullptr, &w);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  Saved sv;
+  if (saved) {
+    if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
+  }
   int sms = 0;
   if ((st = device_info(&sms)) != FLCE_OK) return st;
   carve_fwd(p, workspace, &w);
+  if (saved) {
+    carve_saved(p, saved, &sv);
+    w.part_m = sv.part_m;  // the tile maxima are part of the saved state
+  }
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   const bool pair = use_cta_pair();
   CUtensorMap mx, mw;
-  if (!encode_2d(&mx, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM) ||
-      !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN))
+  if (!encode_2d(&mx, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM, p->input_fp16 != 0) ||
+      !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN,
+                 p->input_fp16 != 0))
     return FLCE_ERR_CUDA;
 
   Tracer tr{trace, s};
   if (!tr.begin()) return FLCE_ERR_CUDA;
-  GemmGeom g = geom(N, V, H);
+  const bool f16 = p->input_fp16 != 0;
+  GemmGeom g = geom(N, V, H, f16);
   FwdLseArgs ea;
-  ea.bias = static_cast<const __nv_bfloat16*>(p->has_bias ? b : nullptr);
+  ea.bias = static_cast<const uint16_t*>(p->has_bias ? b : nullptr);
+  ea.fp16 = f16 ? 1 : 0;
   ea.y = y;
+  ea.y_off = p->vocab_start;
   ea.scale = p->logit_scale;
   ea.V = V;
   ea.Ntok = N;
@@ -272,10 +371,43 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
   ea.part_d = w.part_d;
   ea.part_s = w.part_s;
   ea.zy = w.zy;
-  if (launch_fwd_lse(pair, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
-                     reinterpret_cast<int*>(dev_err), grid_for(g, sms), s) != cudaSuccess ||
-      !tr.after(FLCE_KERNEL_FWD_LSE))
-    return FLCE_ERR_CUDA;
+  cudaError_t le;
+  if (saved) {
+    FwdStoreArgs sa;
+    sa.base = ea;
+    sa.probs = sv.probs;
+    sa.ld_p = sv.ld_p;
+    le = launch_fwd_store(pair, mx, mw, g, sa, p->has_bias != 0, p->label_smoothing > 0.f,
+                          reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
+  } else {
+    le = launch_fwd_lse(pair, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
+                        reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
+  }
+  if (le != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_LSE)) return FLCE_ERR_CUDA;
+
+  if (shard_stats) {
+    ShardStatsArgs sa;
+    sa.part_m = w.part_m;
+    sa.part_d = w.part_d;
+    sa.part_s = w.part_s;
+    sa.zy = w.zy;
+    sa.y = y;
+    sa.N = N;
+    sa.NT = g.tiles_n;
+    sa.vocab_start = p->vocab_start;
+    sa.V = V;
+    sa.V_total = vocab_total(p);
+    sa.ignore_index = p->ignore_index;
+    sa.stats = shard_stats;
+    sa.dev_err = reinterpret_cast<int*>(dev_err);
+    if (p->label_smoothing <= 0.f &&
+        cudaMemsetAsync(shard_stats + 3 * static_cast<size_t>(N), 0, sizeof(float) * N, s) !=
+            cudaSuccess)
+      return FLCE_ERR_CUDA;
+    if (launch_shard_stats(sa, s) != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_MERGE))
+      return FLCE_ERR_CUDA;
+    return FLCE_OK;
+  }
 
   MergeArgs ma;
   ma.part_m = w.part_m;
@@ -285,7 +417,7 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
   ma.y = y;
   ma.N = N;
   ma.NT = g.tiles_n;
-  ma.V = V;
+  ma.V = static_cast<int>(vocab_total(p));
   ma.ignore_index = p->ignore_index;
   ma.eps = p->label_smoothing;
   ma.lam = p->lse_square_scale;
@@ -302,7 +434,7 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
   return FLCE_OK;
 }
 
-flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const float* lse,
+extern "C" flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const float* lse,
                             const void* x, const void* W, const void* b, const int64_t* y,
                             void* dx, void* dW, void* db, void* workspace, size_t workspace_bytes,
                             int32_t* dev_err, void* stream) {
@@ -310,13 +442,37 @@ flce_status_t flce_backward(const flce_params_t* p, const float* dloss, const fl
                               dev_err, stream, nullptr);
 }
 
-flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, const float* lse,
-                                   const void* x, const void* W, const void* b, const int64_t* y,
-                                   void* dx, void* dW, void* db, void* workspace,
-                                   size_t workspace_bytes, int32_t* dev_err, void* stream,
-                                   flce_trace_t* trace) {
+extern "C" flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss,
+                                              const float* lse, const void* x, const void* W,
+                                              const void* b, const int64_t* y, void* dx, void* dW,
+                                              void* db, void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, void* stream,
+                                              flce_trace_t* trace) {
+  return backward_impl(p, dloss, lse, nullptr, 0, x, W, b, y, dx, dW, db, workspace,
+                       workspace_bytes, dev_err, stream, trace);
+}
+
+extern "C" flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss,
+                                             const float* lse, const void* saved,
+                                             size_t saved_bytes, const void* x, const void* W,
+                                             const void* b, const int64_t* y, void* dx, void* dW,
+                                             void* db, void* workspace, size_t workspace_bytes,
+                                             int32_t* dev_err, void* stream,
+                                             flce_trace_t* trace) {
+  if (!saved && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return backward_impl(p, dloss, lse, saved, saved_bytes, x, W, b, y, dx, dW, db, workspace,
+                       workspace_bytes, dev_err, stream, trace);
+}
+
+static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, const float* lse,
+                                   const void* saved, size_t saved_bytes, const void* x,
+                                   const void* W, const void* b, const int64_t* y, void* dx,
+                                   void* dW, void* db, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_err, void* stream, flce_trace_t* trace,
+                                   bool shard) {
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
+  if (shard ? p->vocab_total == 0 : !whole_vocab(p)) return FLCE_ERR_INVALID_ARG;
   if (!dW || (p->has_bias && !db)) return FLCE_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t dw_bytes = static_cast<size_t>(p->V) * p->H * (p->dW_fp32 ? 4 : 2);
@@ -335,6 +491,12 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
   BwdWs w;
   const size_t need = carve_bwd(p, nullptr, &w);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  Saved sv;
+  if (saved) {
+    if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
+    carve_saved(p, const_cast<void*>(saved), &sv);
+  }
   int sms = 0;
   if ((st = device_info(&sms)) != FLCE_OK) return st;
   carve_bwd(p, workspace, &w);
@@ -352,37 +514,66 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
   pa.lse = lse;
   pa.y = y;
   pa.N = N;
-  pa.V = V;
   pa.ignore_index = p->ignore_index;
+  pa.V = static_cast<int>(vocab_total(p));
   pa.eps = p->label_smoothing;
   pa.lam = p->lse_square_scale;
   pa.scale = p->logit_scale;
   pa.reduction = p->reduction;
   pa.coef = w.coef;
+  pa.fp16 = p->input_fp16;
+  pa.dl_scale = w.dl_scale;
   pa.dev_err = derr;
   if (launch_prep(pa, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_PREP)) return FLCE_ERR_CUDA;
 
+  const bool f16 = p->input_fp16 != 0;
   CUtensorMap mx_k, mw_k, mx_mn, mw_mn;
-  if (!encode_2d(&mx_k, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM) ||
-      !encode_2d(&mw_k, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN) ||
-      !encode_2d(&mx_mn, x, H, N, static_cast<uint64_t>(H) * 2, 64, kBK) ||
-      !encode_2d(&mw_mn, W, H, V, static_cast<uint64_t>(H) * 2, 64, kBK))
+  if (!encode_2d(&mx_k, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM, f16) ||
+      !encode_2d(&mw_k, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN, f16) ||
+      !encode_2d(&mx_mn, x, H, N, static_cast<uint64_t>(H) * 2, 64, kBK, f16) ||
+      !encode_2d(&mw_mn, W, H, V, static_cast<uint64_t>(H) * 2, 64, kBK, f16))
     return FLCE_ERR_CUDA;
 
   for (int blk = 0; blk < nblk; ++blk) {
     const int v0 = static_cast<int>(blk * bv);
     const int Vb = static_cast<int>(V - v0 < bv ? V - v0 : bv);
     CUtensorMap mdl_k, mdl_mn;
-    if (!encode_2d(&mdl_k, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, kBK, kBM) ||
-        !encode_2d(&mdl_mn, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, 64, kBK))
+    if (!encode_2d(&mdl_k, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, kBK, kBM, f16) ||
+        !encode_2d(&mdl_mn, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, 64, kBK, f16))
       return FLCE_ERR_CUDA;
 
-    // Recompute the block's logits and form dL (bf16) and db partials.
-    GemmGeom g1 = geom(N, Vb, H);
+    // Recompute the block's logits (or read the stored probabilities) and
+    // form dL (bf16) and db partials.
+    int db_parts = 0;
+    if (saved) {
+      ConvertArgs ca;
+      ca.probs = sv.probs;
+      ca.ld_p = sv.ld_p;
+      ca.part_m = sv.part_m;
+      ca.coef = w.coef;
+      ca.y = y;
+      ca.y_off = p->vocab_start;
+      ca.N = N;
+      ca.v0 = v0;
+      ca.Vb = Vb;
+      ca.dL = w.dL;
+      ca.ld_dL = static_cast<int>(bv);
+      ca.fp16 = p->input_fp16;
+      ca.dl_scale = w.dl_scale;
+      ca.db_part = w.db_part;
+      ca.ld_db = static_cast<int>(bv);
+      if (launch_convert(ca, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_DLOGITS))
+        return FLCE_ERR_CUDA;
+      db_parts = convert_db_parts(N);
+    }
+    GemmGeom g1 = geom(N, Vb, H, f16);
     g1.b_mn_off = v0;
     DlogitsArgs da;
-    da.bias = static_cast<const __nv_bfloat16*>(p->has_bias ? b : nullptr);
+    da.bias = static_cast<const uint16_t*>(p->has_bias ? b : nullptr);
+    da.fp16 = p->input_fp16;
+    da.dl_scale = w.dl_scale;
     da.y = y;
+    da.y_off = p->vocab_start;
     da.coef = w.coef;
     da.scale = p->logit_scale;
     da.V = V;
@@ -393,22 +584,27 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
     da.ld_dL = static_cast<int>(bv);
     da.db_part = w.db_part;
     da.ld_db = static_cast<int>(bv);
-    if (launch_dlogits(pair, mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms), s) !=
-            cudaSuccess ||
-        !tr.after(FLCE_KERNEL_BWD_DLOGITS))
-      return FLCE_ERR_CUDA;
+    if (!saved) {
+      if (launch_dlogits(pair, mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms),
+                         s) != cudaSuccess ||
+          !tr.after(FLCE_KERNEL_BWD_DLOGITS))
+        return FLCE_ERR_CUDA;
+      db_parts = g1.tiles_m * 4;
+    }
     if (p->has_bias &&
-        (launch_db_finalize(w.db_part, g1.tiles_m * 4, static_cast<int>(bv), v0, Vb, db,
-                            p->db_fp32 != 0, s) != cudaSuccess ||
+        (launch_db_finalize(w.db_part, db_parts, static_cast<int>(bv), v0, Vb, db,
+                            p->db_fp32 != 0, f16, s) != cudaSuccess ||
          !tr.after(FLCE_KERNEL_BWD_DB)))
       return FLCE_ERR_CUDA;
 
     // dW block: one GEMM over all tokens (M = vocab rows, K = tokens).
-    GemmGeom g2 = geom(Vb, H, N);
+    GemmGeom g2 = geom(Vb, H, N, f16);
     g2.raster_m_inner = 0;
     DwArgs wa;
     wa.out = dW;
     wa.out_bf16 = p->dW_fp32 ? 0 : 1;
+    wa.fp16 = p->input_fp16;
+    wa.acc_scale = w.dl_scale + 1;
     wa.ld = H;
     wa.row0 = v0;
     wa.Mrows = Vb;
@@ -418,12 +614,15 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
       return FLCE_ERR_CUDA;
 
     // dx += dL_blk W_blk (K = the block's vocab rows).
-    GemmGeom g3 = geom(N, H, Vb);
+    GemmGeom g3 = geom(N, H, Vb, f16);
     g3.b_k_off = v0;
     g3.raster_m_inner = 0;
     DxArgs xa;
     xa.acc = w.dx_acc;
-    xa.out = static_cast<__nv_bfloat16*>(dx);
+    xa.out = static_cast<uint16_t*>(dx);
+    xa.out_f32 = shard ? 1 : 0;
+    xa.fp16 = p->input_fp16;
+    xa.acc_scale = w.dl_scale + 1;
     xa.ld = H;
     xa.Ntok = N;
     xa.Ncols = H;
@@ -434,6 +633,91 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
       return FLCE_ERR_CUDA;
   }
   return FLCE_OK;
+}
+
+extern "C" {
+
+flce_status_t flce_forward_shard(const flce_params_t* p, const void* x, const void* W,
+                                 const void* b, const int64_t* y, float* stats, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  if (!stats && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return forward_impl(p, x, W, b, y, nullptr, nullptr, nullptr, 0, workspace, workspace_bytes,
+                      dev_err, stream, nullptr, stats);
+}
+
+flce_status_t flce_shard_rescale(const flce_params_t* p, float* stats, const float* global_max,
+                                 void* stream) {
+  flce_status_t st = check_params(p);
+  if (st != FLCE_OK) return st;
+  if (p->N == 0) return FLCE_OK;
+  if (!stats || !global_max) return FLCE_ERR_INVALID_ARG;
+  return launch_shard_rescale(stats, global_max, static_cast<int>(p->N),
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FLCE_OK
+             : FLCE_ERR_CUDA;
+}
+
+flce_status_t flce_loss_from_stats(const flce_params_t* p, const float* stats, const int64_t* y,
+                                   float* loss, float* lse, void* workspace,
+                                   size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  flce_status_t st = check_params(p);
+  if (st != FLCE_OK) return st;
+  if (!loss) return FLCE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int N = static_cast<int>(p->N);
+  if (N == 0) {
+    if (p->reduction != FLCE_REDUCTION_NONE &&
+        cudaMemsetAsync(loss, 0, sizeof(float), s) != cudaSuccess)
+      return FLCE_ERR_CUDA;
+    return FLCE_OK;
+  }
+  if (!stats || !y || !lse || !workspace) return FLCE_ERR_INVALID_ARG;
+  const int nblk = cdiv(N, kMergeThreads);
+  Carver c(workspace, 0);
+  double* blk_sum = c.take<double>(nblk);
+  int* blk_cnt = c.take<int>(nblk);
+  if (workspace_bytes < c.used()) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  MergeArgs ma;
+  ma.part_m = stats;
+  ma.part_d = stats + N;
+  ma.zy = stats + 2 * static_cast<size_t>(N);
+  ma.part_s = p->label_smoothing > 0.f ? stats + 3 * static_cast<size_t>(N) : nullptr;
+  ma.y = y;
+  ma.N = N;
+  ma.NT = 1;
+  ma.V = static_cast<int>(vocab_total(p));
+  ma.ignore_index = p->ignore_index;
+  ma.eps = p->label_smoothing;
+  ma.lam = p->lse_square_scale;
+  ma.reduction = p->reduction;
+  ma.lse = lse;
+  ma.loss = loss;
+  ma.blk_sum = blk_sum;
+  ma.blk_cnt = blk_cnt;
+  ma.dev_err = reinterpret_cast<int*>(dev_err);
+  if (launch_merge(ma, s) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (p->reduction != FLCE_REDUCTION_NONE && launch_finalize(ma, s) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return FLCE_OK;
+}
+
+flce_status_t flce_backward_shard(const flce_params_t* p, const float* dloss, const float* lse,
+                                  const void* x, const void* W, const void* b, const int64_t* y,
+                                  float* dx_partial, void* dW, void* db, void* workspace,
+                                  size_t workspace_bytes, int32_t* dev_err, void* stream) {
+  return backward_impl(p, dloss, lse, nullptr, 0, x, W, b, y, dx_partial, dW, db, workspace,
+                       workspace_bytes, dev_err, stream, nullptr, true);
+}
+
+flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_fp16,
+                            void* stream) {
+  if (n < 0 || (n > 0 && (!src || !dst)) || (dst_fp16 != 0 && dst_fp16 != 1))
+    return FLCE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(dst)) return FLCE_ERR_ALIGNMENT;
+  return launch_cast16(src, static_cast<uint16_t*>(dst), n, dst_fp16 != 0,
+                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FLCE_OK
+             : FLCE_ERR_CUDA;
 }
 
 flce_status_t flce_read_device_error(int32_t* dev_err, void* stream, int32_t* host_err) {

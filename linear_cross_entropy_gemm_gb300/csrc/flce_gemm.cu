@@ -83,6 +83,16 @@ cudaError_t launch_fwd_lse(bool pair, const CUtensorMap& a, const CUtensorMap& b
                     : launch_any<FwdLseEpi<false, false>>(pair, a, b, g, ea, dev_err, grid, st);
 }
 
+cudaError_t launch_fwd_store(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                             const GemmGeom& g, const FwdStoreArgs& ea, bool has_bias,
+                             bool has_smooth, int* dev_err, int grid, cudaStream_t st) {
+  if (has_bias)
+    return has_smooth ? launch_any<FwdStoreEpi<true, true>>(pair, a, b, g, ea, dev_err, grid, st)
+                      : launch_any<FwdStoreEpi<true, false>>(pair, a, b, g, ea, dev_err, grid, st);
+  return has_smooth ? launch_any<FwdStoreEpi<false, true>>(pair, a, b, g, ea, dev_err, grid, st)
+                    : launch_any<FwdStoreEpi<false, false>>(pair, a, b, g, ea, dev_err, grid, st);
+}
+
 cudaError_t launch_dlogits(bool pair, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const DlogitsArgs& ea, bool has_bias, int* dev_err,
                            int grid, cudaStream_t st) {

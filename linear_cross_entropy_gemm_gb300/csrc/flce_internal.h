@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "gemm_engine.cuh"
@@ -59,11 +60,55 @@ struct PrepArgs {
   float eps, lam, scale;
   int reduction;
   float4* coef;
+  int fp16;          // operands are fp16: choose a power-of-two dL scale
+  float* dl_scale;   // out [2]: factor applied to dL before rounding, and its inverse
   int* dev_err;
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 
+// Stored-probability backward: fp16 q [N, ld_p] and tile maxima part_m
+// [tiles_v, N] -> bf16 dL block [N, ld_dL] and db partials [ceil(N/32), ld_db].
+struct ConvertArgs {
+  const __half* probs;
+  int ld_p;
+  const float* part_m;
+  const float4* coef;
+  const int64_t* y;
+  int64_t y_off;
+  int N, v0, Vb;
+  uint16_t* dL;    // bf16 or fp16 (fp16 = 1)
+  int ld_dL;
+  int fp16;
+  const float* dl_scale;
+  float* db_part;  // null without a bias
+  int ld_db;
+};
+cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st);
+int convert_db_parts(int N);
+
+struct FwdStoreArgs;
+cudaError_t launch_fwd_store(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+                             const GemmGeom& g, const FwdStoreArgs& ea, bool has_bias,
+                             bool has_smooth, int* dev_err, int grid, cudaStream_t st);
+
+// Vocabulary shards: local partials -> stats [4, N] = (m2, d, z_y or 0, sum z);
+// rescale d by 2^(m2 - M) against the all-shard max M; fp32 -> bf16 cast.
+struct ShardStatsArgs {
+  const float* part_m;
+  const float* part_d;
+  const float* part_s;  // null without smoothing
+  const float* zy;
+  const int64_t* y;
+  int N, NT;
+  int64_t vocab_start, V, V_total, ignore_index;
+  float* stats;
+  int* dev_err;
+};
+cudaError_t launch_shard_stats(const ShardStatsArgs& a, cudaStream_t st);
+cudaError_t launch_shard_rescale(float* stats, const float* gmax, int N, cudaStream_t st);
+cudaError_t launch_cast16(const float* src, uint16_t* dst, int64_t n, bool fp16, cudaStream_t st);
+
 cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, int Vb, void* db,
-                               bool db_fp32, cudaStream_t st);
+                               bool db_fp32, bool fp16, cudaStream_t st);
 
 }  // namespace flce

@@ -5,6 +5,7 @@
 //   prep      : per-token backward coefficients (upstream gradient, z-loss,
 //               smoothing) so the dlogits epilogue is a couple of FMAs
 //   db        : ordered sum of the per-warp bias-gradient partials
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "flce_internal.h"
@@ -122,11 +123,16 @@ cudaError_t launch_finalize(const MergeArgs& a, cudaStream_t st) {
 // One block: count the non-ignored tokens, then per token
 //   g    = dloss (sum) | dloss / total (mean) | dloss[n] (none); 0 if ignored
 //   coef = (lse log2e, s g (1 + 2 lam lse), s g eps / V, s g (1 - eps)).
+// With fp16 operands dL is stored scaled by 2^k so that its bound
+// max_n (|a_n| + |c_n| + |t_n|) (p <= 1) sits near 2^14: large loss scales do
+// not overflow fp16 and small gradients do not flush to zero. The backward
+// GEMM epilogues multiply by 2^-k in fp32 (exact).
 __global__ void __launch_bounds__(1024) prep_kernel(const PrepArgs a) {
   double unused = 0.0;
   int cnt = 0;
   for (int i = threadIdx.x; i < a.N; i += blockDim.x) cnt += (a.y[i] != a.ignore_index);
   block_sum(unused, cnt);
+  float bound = 0.f;
   __shared__ float g_all;
   if (threadIdx.x == 0) {
     const float d0 = a.dloss[0];
@@ -145,8 +151,28 @@ __global__ void __launch_bounds__(1024) prep_kernel(const PrepArgs a) {
     }
     const float lse = a.lse[i];
     const float sg = a.scale * g;
-    a.coef[i] = make_float4(lse * kLog2eF, sg * (1.f + 2.f * a.lam * lse), sg * (a.eps / a.V),
-                            sg * (1.f - a.eps));
+    const float4 cf = make_float4(lse * kLog2eF, sg * (1.f + 2.f * a.lam * lse),
+                                  sg * (a.eps / a.V), sg * (1.f - a.eps));
+    a.coef[i] = cf;
+    bound = fmaxf(bound, fabsf(cf.y) + fabsf(cf.z) + fabsf(cf.w));
+  }
+  // Block max of the bound (fixed order) -> the dL scale.
+  __shared__ float smax[32];
+  for (int o = 16; o > 0; o >>= 1) bound = fmaxf(bound, __shfl_xor_sync(0xffffffffu, bound, o));
+  if ((threadIdx.x & 31) == 0) smax[threadIdx.x >> 5] = bound;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) mx = fmaxf(mx, smax[w]);
+    int k = 0;
+    if (a.fp16 && mx > 0.f && mx < INFINITY) {
+      int e;
+      frexpf(mx, &e);        // mx = f 2^e, f in [0.5, 1)
+      k = 14 - e;            // bound * 2^k in [2^13, 2^14)
+      k = max(-100, min(100, k));
+    }
+    a.dl_scale[0] = ldexpf(1.f, k);
+    a.dl_scale[1] = ldexpf(1.f, -k);
   }
 }
 
@@ -156,7 +182,7 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
 }
 
 __global__ void db_finalize_kernel(const float* __restrict__ part, int parts, int ld, int v0,
-                                   int Vb, void* db, int db_fp32) {
+                                   int Vb, void* db, int db_fp32, int fp16) {
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= Vb) return;
   float s = 0.f;
@@ -164,13 +190,151 @@ __global__ void db_finalize_kernel(const float* __restrict__ part, int parts, in
   if (db_fp32)
     reinterpret_cast<float*>(db)[v0 + c] = s;
   else
-    reinterpret_cast<__nv_bfloat16*>(db)[v0 + c] = __float2bfloat16_rn(s);
+    reinterpret_cast<uint16_t*>(db)[v0 + c] =
+        static_cast<uint16_t>(pack_16x2(s, 0.f, fp16 != 0) & 0xFFFFu);
 }
 
 cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, int Vb, void* db,
-                               bool db_fp32, cudaStream_t st) {
+                               bool db_fp32, bool fp16, cudaStream_t st) {
   db_finalize_kernel<<<(Vb + 255) / 256, 256, 0, st>>>(db_part, parts, ld, v0, Vb, db,
-                                                       db_fp32 ? 1 : 0);
+                                                       db_fp32 ? 1 : 0, fp16 ? 1 : 0);
+  return cudaGetLastError();
+}
+
+// Stored-probability backward: dL[n, v] = a_n q[n, v] 2^(m_t(n) - lse2_n)
+//   - c_n - t_n [v == y_n] for the vocab block [v0, v0 + Vb), q being the
+// forward's fp16 2^(z log2e - m_t). One CTA covers 32 tokens x one 256-column
+// vocab tile (one m_t per token); thread i owns columns 2i, 2i + 1 and also
+// writes their fp32 column sums over the 32 tokens (db partials, row blockIdx.y).
+constexpr int kConvRows = 32;
+__global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs a) {
+  __shared__ float s_scale[kConvRows], s_c[kConvRows], s_t[kConvRows];
+  __shared__ int s_ty[kConvRows];
+  const int tile = blockIdx.x;                  // 256-column tile inside the block
+  const int r0 = blockIdx.y * kConvRows;
+  const int colb = tile * 256 + threadIdx.x * 2;  // block-relative column
+  if (threadIdx.x < kConvRows) {
+    const int r = r0 + threadIdx.x;
+    float sc = 0.f, c = 0.f, t = 0.f;
+    int ty = -1;
+    if (r < a.N) {
+      const float4 cf = a.coef[r];
+      const float mt = a.part_m[static_cast<size_t>(a.v0 / 256 + tile) * a.N + r];
+      sc = cf.y * exp2f(mt - cf.x);
+      c = cf.z;
+      t = cf.w;
+      const int64_t yv = a.y[r] - a.y_off;
+      const int64_t lo = static_cast<int64_t>(a.v0) + tile * 256;
+      if (yv >= lo && yv < lo + 256) ty = static_cast<int>(yv - a.v0);
+    }
+    s_scale[threadIdx.x] = sc;
+    s_c[threadIdx.x] = c;
+    s_t[threadIdx.x] = t;
+    s_ty[threadIdx.x] = ty;
+  }
+  __syncthreads();
+  const bool ok0 = colb < a.Vb, ok1 = colb + 1 < a.Vb;
+  const float dls = a.dl_scale[0];
+  float sum0 = 0.f, sum1 = 0.f;
+  const int rows = min(kConvRows, a.N - r0);
+  for (int i = 0; i < rows; ++i) {
+    const size_t r = static_cast<size_t>(r0 + i);
+    const __half2 q = *reinterpret_cast<const __half2*>(a.probs + r * a.ld_p + a.v0 + colb);
+    const float2 qf = __half22float2(q);
+    float d0 = fmaf(s_scale[i], qf.x, -s_c[i]) - (colb == s_ty[i] ? s_t[i] : 0.f);
+    float d1 = fmaf(s_scale[i], qf.y, -s_c[i]) - (colb + 1 == s_ty[i] ? s_t[i] : 0.f);
+    d0 = ok0 ? d0 : 0.f;
+    d1 = ok1 ? d1 : 0.f;
+    sum0 += d0;
+    sum1 += d1;
+    *reinterpret_cast<uint32_t*>(a.dL + r * a.ld_dL + colb) =
+        pack_16x2(d0 * dls, d1 * dls, a.fp16 != 0);
+  }
+  if (a.db_part) {
+    float* dp = a.db_part + static_cast<size_t>(blockIdx.y) * a.ld_db + colb;
+    if (ok0) dp[0] = sum0;
+    if (ok1) dp[1] = sum1;
+  }
+}
+
+cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st) {
+  dim3 grid((a.Vb + 255) / 256, (a.N + kConvRows - 1) / kConvRows);
+  probs_to_dlogits_kernel<<<grid, 128, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+int convert_db_parts(int N) { return (N + kConvRows - 1) / kConvRows; }
+
+// One shard's per-token statistics over its vocabulary rows: the (m, d)
+// merge of its tile partials, its sum of z, and z_y when the target falls in
+// the shard (0 otherwise, so a SUM across shards yields z_y exactly once).
+__global__ void __launch_bounds__(256) shard_stats_kernel(const ShardStatsArgs a) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= a.N) return;
+  float M = -INFINITY, D = 0.f, S = 0.f;
+  for (int t = 0; t < a.NT; ++t) {
+    const size_t o = static_cast<size_t>(t) * a.N + row;
+    const float m = a.part_m[o];
+    const float d = a.part_d[o];
+    const float nm = fmaxf(M, m);
+    D = D * fast_exp2(M - nm) + d * fast_exp2(m - nm);
+    M = nm;
+    if (a.part_s) S += a.part_s[o];
+  }
+  const int64_t yv = a.y[row];
+  float zy = 0.f;
+  if (yv != a.ignore_index) {
+    if (yv < 0 || yv >= a.V_total) {
+      if (a.dev_err) atomicOr(a.dev_err, kDevErrTarget);
+    } else if (yv >= a.vocab_start && yv < a.vocab_start + a.V) {
+      zy = a.zy[row];
+    }
+  }
+  a.stats[row] = M;
+  a.stats[static_cast<size_t>(a.N) + row] = D;
+  a.stats[2 * static_cast<size_t>(a.N) + row] = zy;
+  a.stats[3 * static_cast<size_t>(a.N) + row] = S;
+}
+
+cudaError_t launch_shard_stats(const ShardStatsArgs& a, cudaStream_t st) {
+  shard_stats_kernel<<<(a.N + 255) / 256, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// d <- d 2^(m - M), m <- M, with M the maximum of m over all shards.
+__global__ void shard_rescale_kernel(float* stats, const float* gmax, int N) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= N) return;
+  const float M = gmax[row];
+  const float m = stats[row];
+  stats[static_cast<size_t>(N) + row] *= fast_exp2(m - M);
+  stats[row] = M;
+}
+
+cudaError_t launch_shard_rescale(float* stats, const float* gmax, int N, cudaStream_t st) {
+  shard_rescale_kernel<<<(N + 255) / 256, 256, 0, st>>>(stats, gmax, N);
+  return cudaGetLastError();
+}
+
+__global__ void cast16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, int64_t n,
+                              int fp16) {
+  const int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 4;
+  if (i + 4 <= n) {
+    const float4 v = *reinterpret_cast<const float4*>(src + i);
+    uint2 o;
+    o.x = pack_16x2(v.x, v.y, fp16 != 0);
+    o.y = pack_16x2(v.z, v.w, fp16 != 0);
+    *reinterpret_cast<uint2*>(dst + i) = o;
+  } else {
+    for (int64_t j = i; j < n; ++j)
+      dst[j] = static_cast<uint16_t>(pack_16x2(src[j], 0.f, fp16 != 0) & 0xFFFFu);
+  }
+}
+
+cudaError_t launch_cast16(const float* src, uint16_t* dst, int64_t n, bool fp16, cudaStream_t st) {
+  const int64_t blocks = (n + 1023) / 1024;
+  if (blocks == 0) return cudaSuccess;
+  cast16_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(src, dst, n, fp16 ? 1 : 0);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,7 @@ struct GemmGeom {
   int b_mn_off, b_k_off;
   int raster_m_inner;     // 1: consecutive tiles advance along M first
   int group;              // >0: tiles walk M inner inside groups of `group` N-tiles
+  int ab_fp16;            // operands are fp16 (else bf16)
 };
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, int& tn) {
@@ -174,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // --------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, kAMN, kBMN);
+      const uint32_t idesc = idesc_f16kind_f32(kBM, kBN, kAMN, kBMN, g.ab_fp16 != 0);
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -374,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       if (leader) {
         // ------------------------------------------- MMA issuer (even CTA)
-        constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN, kAMN, kBMN);
+        const uint32_t idesc = idesc_f16kind_f32(2 * kBM, kBN, kAMN, kBMN, g.ab_fp16 != 0);
         int s = 0;
         uint32_t ph = 0;
         int acc = 0;

@@ -167,12 +167,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, M x N tile.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major,
-                                                      bool b_mn_major) {
+// Instruction descriptor, kind::f16: (bf16 x bf16 or f16 x f16) -> fp32, M x N.
+__host__ __device__ constexpr uint32_t idesc_f16kind_f32(int M, int N, bool a_mn_major,
+                                                         bool b_mn_major, bool fp16) {
   return (1u << 4)                                  // D format: f32
-         | (1u << 7)                                // A format: bf16
-         | (1u << 10)                               // B format: bf16
+         | ((fp16 ? 0u : 1u) << 7)                  // A format: f16 (0) or bf16 (1)
+         | ((fp16 ? 0u : 1u) << 10)                 // B format: same as A
          | (static_cast<uint32_t>(a_mn_major) << 15)  // A major-ness (1 = MN)
          | (static_cast<uint32_t>(b_mn_major) << 16)  // B major-ness (1 = MN)
          | (static_cast<uint32_t>(N >> 3) << 17)      // N / 8
@@ -255,6 +255,26 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two fp32 values -> packed 16-bit pair of the operand type (fp16 or bf16).
+__device__ __forceinline__ uint32_t pack_16x2(float lo, float hi, bool fp16) {
+  return fp16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+}
+// One 16-bit operand-type value (bits) -> fp32.
+__device__ __forceinline__ float unpack_16(uint32_t bits16, bool fp16) {
+  if (fp16) {
+    float f;
+    asm("{\n\t.reg .f16 h;\n\tmov.b16 h, %1;\n\tcvt.f32.f16 %0, h;\n\t}"
+        : "=f"(f)
+        : "h"(static_cast<unsigned short>(bits16)));
+    return f;
+  }
+  return __uint_as_float(bits16 << 16);
 }
 
 }  // namespace flce

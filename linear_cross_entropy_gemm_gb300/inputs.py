@@ -62,15 +62,28 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-def normal_bf16(seed: int, stream: int, shape, std: float) -> np.ndarray:
-    """N(0, std^2) samples rounded to bf16; returns uint16 bit patterns."""
+def f32_to_f16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE fp16 (round to nearest, ties to even)."""
+    return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def bits_to_f64(bits: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    """Exact widening of bf16 or fp16 bit patterns to float64."""
+    if dtype == "fp16":
+        return bits.view(np.float16).astype(np.float64)
+    return bf16_bits_to_f64(bits)
+
+
+def normal_bf16(seed: int, stream: int, shape, std: float, dtype: str = "bf16") -> np.ndarray:
+    """N(0, std^2) samples rounded to bf16 (or fp16); returns uint16 bit patterns."""
     n = int(np.prod(shape))
     g = _rng(seed, stream)
     out = np.empty(n, dtype=np.uint16)
     s = np.float32(std)
+    conv = f32_to_f16_bits if dtype == "fp16" else f32_to_bf16_bits
     for i in range(0, n, _CHUNK):
         k = min(_CHUNK, n - i)
-        out[i:i + k] = f32_to_bf16_bits(g.standard_normal(k, dtype=np.float32) * s)
+        out[i:i + k] = conv(g.standard_normal(k, dtype=np.float32) * s)
     return out.reshape(shape)
 
 
@@ -117,6 +130,8 @@ class Workload:
     logit_scale: float = 1.0
     reduction: str = "mean"
     dloss: str = "one"                  # "one" | "normal_scalar" | "normal_per_token"
+    dtype: str = "bf16"                 # operand type of x, W, b: "bf16" | "fp16"
+    dloss_scale: float = 1.0            # multiplies dloss (a loss scale, e.g. 65536)
 
     @property
     def has_bias(self) -> bool:
@@ -151,7 +166,8 @@ WORKLOADS = {
 
 @dataclasses.dataclass
 class Inputs:
-    """Host arrays of one workload. bf16 tensors are held as uint16 bit patterns."""
+    """Host arrays of one workload. bf16 / fp16 tensors are held as uint16 bit
+    patterns (the workload's dtype says which)."""
     wl: Workload
     x: np.ndarray            # uint16 [N, H]
     W: np.ndarray            # uint16 [V, H]
@@ -161,9 +177,9 @@ class Inputs:
 
 
 def make_inputs(wl: Workload) -> Inputs:
-    x = normal_bf16(wl.seed, _S_X, (wl.N, wl.H), wl.x_std)
-    W = normal_bf16(wl.seed, _S_W, (wl.V, wl.H), wl.w_std)
-    b = normal_bf16(wl.seed, _S_B, (wl.V,), wl.b_std) if wl.has_bias else None
+    x = normal_bf16(wl.seed, _S_X, (wl.N, wl.H), wl.x_std, wl.dtype)
+    W = normal_bf16(wl.seed, _S_W, (wl.V, wl.H), wl.w_std, wl.dtype)
+    b = normal_bf16(wl.seed, _S_B, (wl.V,), wl.b_std, wl.dtype) if wl.has_bias else None
     if wl.target_dist == "uniform":
         y = uniform_targets(wl.seed, wl.N, wl.V)
     elif wl.target_dist == "zipf":
@@ -182,6 +198,8 @@ def make_inputs(wl: Workload) -> Inputs:
         raise ValueError(wl.dloss)
     if wl.reduction != "none" and dloss.size != 1:
         raise ValueError("a reduced loss takes a scalar upstream gradient")
+    if wl.dloss_scale != 1.0:
+        dloss = (dloss * np.float32(wl.dloss_scale)).astype(np.float32)
     return Inputs(wl, x, W, b, y, dloss)
 
 

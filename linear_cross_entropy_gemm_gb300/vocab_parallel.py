@@ -1,0 +1,151 @@
+"""Vocabulary-parallel fused linear cross-entropy (DeepSpeed PR #8792).
+
+Each rank holds the rows [vocab_start, vocab_start + V_local) of the LM head
+(uneven shards allowed) and the same tokens and targets. Forward: every rank
+folds its logits into per-token statistics (m, d, z_y, sum z) with the
+library's kernels; one MAX all-reduce of m, a rescale of d to the common
+max, and one SUM all-reduce of (d, z_y, sum z) give every rank the
+whole-vocabulary lse and loss. Backward: each rank writes its own dW rows
+and db and an fp32 partial dx; a SUM all-reduce of the fp32 partials comes
+before the single cast to bf16, so partials that would overflow a narrower
+type but cancel across shards stay finite.
+
+The collectives are torch.distributed all-reduces on ``group`` (skipped when
+there is a single rank); ``allreduce`` may replace them (a function
+``allreduce(tensor, op)`` with op "max" or "sum", reducing in place).
+All arithmetic runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+from typing import Callable, Optional
+
+import torch
+
+from . import _lib
+from . import _check_inputs, _ptr, _stream, device_error_word, params, FlceError
+
+AllReduce = Callable[[torch.Tensor, str], None]
+
+
+def _dist_allreduce(group) -> AllReduce:
+    import torch.distributed as dist
+
+    def f(t: torch.Tensor, op: str) -> None:
+        if not dist.is_available() or not dist.is_initialized() or dist.get_world_size(group) == 1:
+            return
+        dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM, group=group)
+    return f
+
+
+def _shard_params(N, H, V_local, vocab_start, vocab_total, has_bias, fp16, opts):
+    return params(N, H, V_local, has_bias=has_bias, vocab_start=vocab_start,
+                  vocab_total=vocab_total, input_fp16=fp16, **opts)
+
+
+def forward_shard(x, W, b, y, *, vocab_start, vocab_total, stream=None, **opts) -> torch.Tensor:
+    """This shard's per-token statistics, a [4, N] fp32 tensor (m, d, z_y, sum z)."""
+    _check_inputs(x, W, b, y)
+    lib = _lib.load()
+    N, H = x.shape
+    p = _shard_params(N, H, W.shape[0], vocab_start, vocab_total, b is not None,
+                      x.dtype == torch.float16, opts)
+    stats = torch.empty(4, N, dtype=torch.float32, device=x.device)
+    ws = torch.empty(max(lib.flce_workspace_size(p, 0), 1), dtype=torch.uint8, device=x.device)
+    st = lib.flce_forward_shard(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(stats), _ptr(ws),
+                                ws.numel(), _ptr(device_error_word(x.device)), _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_forward_shard")
+    return stats
+
+
+def rescale(stats: torch.Tensor, global_max: torch.Tensor, stream=None) -> None:
+    """d <- d 2^(m - M), m <- M (in place), M the all-shard max of m."""
+    N = stats.shape[1]
+    p = params(N, 8, 1)
+    st = _lib.load().flce_shard_rescale(p, _ptr(stats), _ptr(global_max), _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_shard_rescale")
+
+
+def merge_stats(stats: torch.Tensor, allreduce: AllReduce,
+                rescale_fn: Callable[[torch.Tensor, torch.Tensor], None] = rescale) -> torch.Tensor:
+    """The exchange step: MAX all-reduce of m, rescale of d, SUM all-reduce of
+    (d, z_y, sum z). After it every rank holds the whole-vocabulary stats."""
+    gmax = stats[0].clone()
+    allreduce(gmax, "max")
+    rescale_fn(stats, gmax)
+    rest = stats[1:]
+    allreduce(rest, "sum")
+    return stats
+
+
+def loss_from_stats(stats, y, *, vocab_total, H, stream=None, **opts):
+    """loss and lse from merged statistics (as flce_forward on the whole vocabulary)."""
+    lib = _lib.load()
+    N = stats.shape[1]
+    p = params(N, H, vocab_total, **opts)
+    red = opts.get("reduction", "mean")
+    loss = torch.empty(N if red == "none" else 1, dtype=torch.float32, device=stats.device)
+    lse = torch.empty(N, dtype=torch.float32, device=stats.device)
+    ws = torch.empty(max(lib.flce_workspace_size(p, 0), 1), dtype=torch.uint8, device=stats.device)
+    st = lib.flce_loss_from_stats(p, _ptr(stats), _ptr(y), _ptr(loss), _ptr(lse), _ptr(ws),
+                                  ws.numel(), _ptr(device_error_word(stats.device)),
+                                  _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_loss_from_stats")
+    return (loss if red == "none" else loss.view(())), lse
+
+
+def backward_shard(dloss, lse, x, W, b, y, *, vocab_start, vocab_total, stream=None,
+                   dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0, **opts):
+    """This shard's dW rows, db, and its fp32 partial dx [N, H]."""
+    _check_inputs(x, W, b, y)
+    lib = _lib.load()
+    N, H = x.shape
+    V = W.shape[0]
+    p = params(N, H, V, has_bias=b is not None, vocab_start=vocab_start, vocab_total=vocab_total,
+               dW_fp32=dW_dtype == torch.float32, db_fp32=db_dtype == torch.float32,
+               bwd_vocab_block=bwd_vocab_block, input_fp16=x.dtype == torch.float16, **opts)
+    dev = x.device
+    dloss = dloss.reshape(-1).float().contiguous()
+    dx = torch.empty(N, H, dtype=torch.float32, device=dev)
+    dW = torch.empty(V, H, dtype=dW_dtype, device=dev)
+    db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
+    ws = torch.empty(max(lib.flce_workspace_size(p, 1), 1), dtype=torch.uint8, device=dev)
+    st = lib.flce_backward_shard(p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y),
+                                 _ptr(dx), _ptr(dW), _ptr(db), _ptr(ws), ws.numel(),
+                                 _ptr(device_error_word(dev)), _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_backward_shard")
+    return dx, dW, db
+
+
+def cast16(src: torch.Tensor, dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """fp32 -> bf16 / fp16 (round to nearest even) in the library's kernel."""
+    dst = torch.empty(src.shape, dtype=dtype, device=src.device)
+    st = _lib.load().flce_cast_f32(_ptr(src), _ptr(dst), src.numel(),
+                                   1 if dtype == torch.float16 else 0, _stream(stream))
+    if st != _lib.FLCE_OK:
+        raise FlceError(st, "flce_cast_f32")
+    return dst
+
+
+def vocab_parallel_forward(x, W_local, b_local, y, *, vocab_start: int, vocab_total: int,
+                           group=None, allreduce: Optional[AllReduce] = None, **opts):
+    """Whole-vocabulary loss and lse on every rank from its vocabulary shard."""
+    ar = allreduce or _dist_allreduce(group)
+    stats = forward_shard(x, W_local, b_local, y, vocab_start=vocab_start,
+                          vocab_total=vocab_total, **opts)
+    merge_stats(stats, ar)
+    return loss_from_stats(stats, y, vocab_total=vocab_total, H=x.shape[1], **opts)
+
+
+def vocab_parallel_backward(dloss, lse, x, W_local, b_local, y, *, vocab_start: int,
+                            vocab_total: int, group=None, allreduce: Optional[AllReduce] = None,
+                            **opts):
+    """bf16 dx (summed over shards in fp32), this shard's dW rows and db."""
+    ar = allreduce or _dist_allreduce(group)
+    dx32, dW, db = backward_shard(dloss, lse, x, W_local, b_local, y, vocab_start=vocab_start,
+                                  vocab_total=vocab_total, **opts)
+    ar(dx32, "sum")
+    return cast16(dx32, x.dtype), dW, db

@@ -17,8 +17,9 @@ GRAD_FROB = 5e-3
 GRAD_MAX = 2.0 ** -7
 
 
-def bf16_dev(bits: np.ndarray, dev) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+def bf16_dev(bits: np.ndarray, dev, dtype: str = "bf16") -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if dtype == "fp16" else torch.bfloat16).to(dev)
 
 
 def opts_of(wl: I.Workload) -> dict:
@@ -31,28 +32,39 @@ class DeviceProblem:
     def __init__(self, inp: I.Inputs, dev="cuda:0"):
         self.inp = inp
         self.dev = torch.device(dev)
-        self.x = bf16_dev(inp.x, self.dev)
-        self.W = bf16_dev(inp.W, self.dev)
-        self.b = None if inp.b is None else bf16_dev(inp.b, self.dev)
+        dt = inp.wl.dtype
+        self.x = bf16_dev(inp.x, self.dev, dt)
+        self.W = bf16_dev(inp.W, self.dev, dt)
+        self.b = None if inp.b is None else bf16_dev(inp.b, self.dev, dt)
         self.y = torch.from_numpy(inp.y).to(self.dev)
         self.dloss = torch.from_numpy(inp.dloss).to(self.dev)
 
-    def run(self, *, dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0, **over):
+    def run(self, *, dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0,
+            store=False, **over):
+        """Forward + backward through the C ABI. store=True uses the
+        stored-probability mode (no logits recompute in the backward)."""
         import linear_cross_entropy_gemm_gb300 as F
         opts = opts_of(self.inp.wl)
         opts.update(over)
-        loss, lse = F.flce_forward(self.x, self.W, self.b, self.y, **opts)
+        wl = self.inp.wl
+        saved = None
+        if store:
+            n = F.flce_saved_size(wl.N, wl.H, wl.V, label_smoothing=opts["label_smoothing"],
+                                  input_fp16=wl.dtype == "fp16")
+            saved = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
+        loss, lse = F.flce_forward(self.x, self.W, self.b, self.y, saved=saved, **opts)
         dx, dW, db = F.flce_backward(self.dloss, lse, self.x, self.W, self.b, self.y,
                                      dW_dtype=dW_dtype, db_dtype=db_dtype,
-                                     bwd_vocab_block=bwd_vocab_block, **opts)
+                                     bwd_vocab_block=bwd_vocab_block, saved=saved, **opts)
         torch.cuda.synchronize(self.dev)
         err = F.flce_read_device_error(self.dev)
         return dict(loss=loss, lse=lse, dx=dx, dW=dW, db=db, err=err)
 
 
 def f64(inp: I.Inputs):
-    return (I.bf16_bits_to_f64(inp.x), I.bf16_bits_to_f64(inp.W),
-            None if inp.b is None else I.bf16_bits_to_f64(inp.b))
+    dt = inp.wl.dtype
+    return (I.bits_to_f64(inp.x, dt), I.bits_to_f64(inp.W, dt),
+            None if inp.b is None else I.bits_to_f64(inp.b, dt))
 
 
 def assert_loss_close(got, ref, what):

@@ -39,8 +39,10 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_params_struct_layout_matches_header():
-    assert ctypes.sizeof(_lib.FlceParams) == 72
+    assert ctypes.sizeof(_lib.FlceParams) == 96
     assert _lib.FlceParams.bwd_vocab_block.offset == 64
+    assert _lib.FlceParams.vocab_total.offset == 80
+    assert _lib.FlceParams.input_fp16.offset == 88
 
 
 def test_status_strings(lib):

@@ -17,10 +17,14 @@ from parity import (DeviceProblem, assert_grad_close, assert_loss_close, f64, op
 pytestmark = pytest.mark.gpu
 
 
-def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.float32):
+MODES = [pytest.param(False, id="recompute"), pytest.param(True, id="stored")]
+
+
+def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.float32,
+               store=False):
     inp = I.make_inputs(wl)
     out = DeviceProblem(inp).run(bwd_vocab_block=bwd_vocab_block, dW_dtype=dW_dtype,
-                                 db_dtype=db_dtype)
+                                 db_dtype=db_dtype, store=store)
     assert out["err"] == 0, f"device error word {out['err']}"
     x64, W64, b64 = f64(inp)
     opts = opts_of(wl)
@@ -35,41 +39,105 @@ def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.
     return out
 
 
-def test_tiny_full():
-    full_check(I.WORKLOADS["tiny"])
+@pytest.mark.parametrize("store", MODES)
+def test_tiny_full(store):
+    full_check(I.WORKLOADS["tiny"], store=store)
 
 
-def test_medium_full_with_bias_smoothing_zloss():
-    full_check(I.WORKLOADS["medium"])
+@pytest.mark.parametrize("store", MODES)
+def test_medium_full_with_bias_smoothing_zloss(store):
+    full_check(I.WORKLOADS["medium"], store=store)
 
 
+@pytest.mark.parametrize("store", MODES)
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-def test_ragged_tails_multi_block(reduction):
+def test_ragged_tails_multi_block(reduction, store):
     # N, H, V not multiples of the 128 x 256 x 64 tile; vocab blocks of 256
     # leave a 1-column last block.
     wl = I.Workload("ragged", N=129, H=72, V=257, seed=21, b_std=0.5, ignore_frac=0.1,
                     label_smoothing=0.2, lse_square_scale=1e-2, logit_scale=1.3,
                     reduction=reduction,
                     dloss="normal_per_token" if reduction == "none" else "normal_scalar")
-    full_check(wl, bwd_vocab_block=256)
+    full_check(wl, bwd_vocab_block=256, store=store)
 
 
-def test_degenerate_single_class_single_token():
+@pytest.mark.parametrize("store", MODES)
+def test_degenerate_single_class_single_token(store):
     wl = I.Workload("v1", N=1, H=8, V=1, seed=22, b_std=1.0, label_smoothing=0.3,
                     lse_square_scale=0.1, reduction="sum")
-    full_check(wl)
+    full_check(wl, store=store)
 
 
-def test_few_tokens_many_vocab_blocks():
+@pytest.mark.parametrize("store", MODES)
+def test_few_tokens_many_vocab_blocks(store):
     wl = I.Workload("wide", N=5, H=64, V=5000, seed=23, x_std=2.0, w_std=0.1,
                     label_smoothing=0.05, reduction="mean")
-    full_check(wl, bwd_vocab_block=1024)
+    full_check(wl, bwd_vocab_block=1024, store=store)
 
 
-def test_bf16_gradients_and_custom_ignore_index():
+@pytest.mark.parametrize("store", MODES)
+def test_bf16_gradients_and_custom_ignore_index(store):
     wl = I.Workload("bf16out", N=200, H=128, V=777, seed=24, b_std=0.1, ignore_frac=0.2,
                     ignore_index=5, reduction="mean")
-    full_check(wl, dW_dtype=torch.bfloat16, db_dtype=torch.bfloat16, bwd_vocab_block=512)
+    full_check(wl, dW_dtype=torch.bfloat16, db_dtype=torch.bfloat16, bwd_vocab_block=512,
+               store=store)
+
+
+def test_large_logits_small_shape_both_modes():
+    # logit std ~45 (x, W, b ~ N(0, 1)): most tile probabilities underflow fp16
+    # in the stored mode; the ones that matter must survive.
+    wl = I.WORKLOADS["large_logit"].with_(N=300, V=3000, H=2048)
+    full_check(wl, bwd_vocab_block=1024, store=False)
+    full_check(wl, bwd_vocab_block=1024, store=True)
+
+
+@pytest.mark.parametrize("store", MODES)
+def test_fp16_operands(store):
+    wl = I.WORKLOADS["medium"].with_(name="medium_fp16", dtype="fp16", N=1000, V=5000)
+    full_check(wl, bwd_vocab_block=2048, store=store,
+               dW_dtype=torch.float16, db_dtype=torch.float16)
+
+
+@pytest.mark.parametrize("store", MODES)
+def test_fp16_loss_scaled_gradients_do_not_overflow(store):
+    # sum reduction with a 65536 loss scale: dlogits reach ~65536 > fp16 max
+    # before the library's power-of-two dL scaling.
+    wl = I.Workload("fp16_scaled", N=400, H=256, V=3000, seed=28, dtype="fp16", x_std=2.0,
+                    w_std=0.5, reduction="sum", dloss_scale=65536.0)
+    full_check(wl, bwd_vocab_block=1024, store=store)
+
+
+@pytest.mark.parametrize("store", MODES)
+def test_fp16_small_gradients_do_not_flush(store):
+    # mean over 4096 tokens of a 30000-way softmax: dlogits ~ 1e-9, below fp16's
+    # smallest subnormal without the library's power-of-two dL scaling.
+    wl = I.Workload("fp16_tiny_grads", N=4096, H=128, V=30000, seed=29, dtype="fp16",
+                    reduction="mean")
+    full_check(wl, store=store)
+
+
+def test_fp16_product_beyond_fp16_range_before_bias():
+    # x W^T ~ 7e4 (> 65504) with a cancelling bias: fp32 accumulation keeps the
+    # logits finite (DeepSpeed PR #8792's fp32-output GEMM lesson).
+    wl = I.Workload("fp16_bigdot", N=64, H=64, V=512, seed=30, dtype="fp16", reduction="mean")
+    inp = I.make_inputs(wl)
+    h16 = lambda v: np.full(1, v, np.float32).astype(np.float16).view(np.uint16)[0]
+    inp.x[:] = h16(32.5)
+    W = np.random.default_rng(3).standard_normal((wl.V, wl.H)).astype(np.float32)
+    inp.W[:] = (32.5 + 0.05 * W).astype(np.float16).view(np.uint16)
+    inp.b = np.full(wl.V, h16(-65504.0), dtype=np.uint16)
+    wl2 = wl.with_(b_std=1.0)
+    inp = I.Inputs(wl2, inp.x, inp.W, inp.b, inp.y, inp.dloss)
+    out = DeviceProblem(inp).run()
+    assert out["err"] == 0
+    x64, W64, b64 = f64(inp)
+    opts = opts_of(wl2)
+    rl, rlse = O.forward(x64, W64, b64, inp.y, **opts)
+    assert np.all(np.isfinite(to_np(out["lse"])))
+    assert_loss_close(to_np(out["loss"]), rl, "fp16 big-dot loss")
+    assert_loss_close(to_np(out["lse"]), rlse, "fp16 big-dot lse")
+    rdx, rdW, rdb = O.backward(inp.dloss.astype(np.float64), x64, W64, b64, inp.y, **opts)
+    assert_grad_close(to_np(out["dW"]), rdW, "fp16 big-dot dW")
 
 
 def test_all_rows_ignored_mean_gives_zero():
@@ -103,26 +171,28 @@ def test_out_of_range_target_sets_device_error():
     assert F.flce_read_device_error() == 0, "error word not cleared"
 
 
-def test_run_to_run_bitwise_determinism():
+@pytest.mark.parametrize("store", MODES)
+def test_run_to_run_bitwise_determinism(store):
     wl = I.WORKLOADS["medium"].with_(N=1000, V=3000)
     p = DeviceProblem(I.make_inputs(wl))
-    a = p.run(bwd_vocab_block=1024)
-    b = p.run(bwd_vocab_block=1024)
+    a = p.run(bwd_vocab_block=1024, store=store)
+    b = p.run(bwd_vocab_block=1024, store=store)
     for k in ("loss", "lse", "dx", "dW", "db"):
         assert torch.equal(a[k], b[k]), f"{k} differs between runs"
 
 
-def test_autograd_module_matches_c_abi():
+@pytest.mark.parametrize("store", MODES)
+def test_autograd_module_matches_c_abi(store):
     wl = I.Workload("module", N=256, H=128, V=1000, seed=27, b_std=0.05, ignore_frac=0.05,
                     label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.9)
     inp = I.make_inputs(wl)
     p = DeviceProblem(inp)
-    ref = p.run()
+    ref = p.run(store=store)
     x = p.x.clone().requires_grad_(True)
     W = p.W.clone().requires_grad_(True)
     b = p.b.clone().requires_grad_(True)
     mod = F.FusedLinearCrossEntropyLoss(label_smoothing=0.1, lse_square_scale=1e-3,
-                                        logit_scale=0.9)
+                                        logit_scale=0.9, recompute=not store)
     loss = mod(x.view(2, 128, 128), p.y.view(2, 128), W, b)
     loss.backward()
     torch.cuda.synchronize()
@@ -145,8 +215,7 @@ def _sampled(name):
     _cache.clear()
     wl = I.WORKLOADS[name]
     inp = I.make_inputs(wl)
-    out = DeviceProblem(inp).run()
-    assert out["err"] == 0, f"device error word {out['err']}"
+    prob = DeviceProblem(inp)
     opts = opts_of(wl)
     x64, W64, b64 = f64(inp)
     lse, zt, sz = O.row_stats(x64, W64, b64, inp.y, ignore_index=wl.ignore_index,
@@ -163,21 +232,26 @@ def _sampled(name):
     dl = inp.dloss.astype(np.float64)
     rdx = O.dx_rows(rows, dl, x64, W64, b64, inp.y, **opts)
     rdW, rdb = O.dW_db_rows(vrows, lse, dl, x64, W64, b64, inp.y, **opts)
-    got = dict(loss=to_np(out["loss"]), lse=to_np(out["lse"]),
-               dx=to_np(out["dx"][torch.from_numpy(rows).to(out["dx"].device)]),
-               dW=to_np(out["dW"][torch.from_numpy(vrows).to(out["dW"].device)]),
-               db=None if out["db"] is None else to_np(out["db"])[vrows])
-    del out
-    torch.cuda.empty_cache()
+    got = {}
+    for store in (False, True):
+        out = prob.run(store=store)
+        assert out["err"] == 0, f"device error word {out['err']}"
+        got[store] = dict(loss=to_np(out["loss"]), lse=to_np(out["lse"]),
+                          dx=to_np(out["dx"][torch.from_numpy(rows).to(out["dx"].device)]),
+                          dW=to_np(out["dW"][torch.from_numpy(vrows).to(out["dW"].device)]),
+                          db=None if out["db"] is None else to_np(out["db"])[vrows])
+        del out
+        torch.cuda.empty_cache()
     res = dict(wl=wl, got=got, ref=dict(loss=ref_loss, lse=lse, dx=rdx, dW=rdW, db=rdb))
     _cache[name] = res
     return res
 
 
+@pytest.mark.parametrize("store", MODES)
 @pytest.mark.parametrize("name", ["llama3_head", "large_logit", "vocab256k"])
-def test_full_size_sampled(name):
+def test_full_size_sampled(name, store):
     r = _sampled(name)
-    g, ref, wl = r["got"], r["ref"], r["wl"]
+    g, ref, wl = r["got"][store], r["ref"], r["wl"]
     assert_loss_close(g["loss"], ref["loss"], f"{name} loss")
     assert_loss_close(g["lse"], ref["lse"], f"{name} lse (all tokens)")
     assert_grad_close(g["dx"], ref["dx"], f"{name} dx (sampled rows)")

@@ -1,0 +1,108 @@
+"""Multi-rank host logic on CPU with the gloo backend (world size 2): the
+benchmark's replicas are timed by the slowest rank. No GPU involved."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+        got = bench.max_over_ranks(10.0 + 7.5 * rank, world, torch.device("cpu"))
+        q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_bench_takes_the_slowest_rank():
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    res = dict(q.get(timeout=10) for _ in range(world))
+    assert res == {0: 17.5, 1: 17.5}
+
+
+def test_single_process_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.25, 1, torch.device("cpu")) == 3.25
+
+
+def _stats_of(z):
+    """Per-token (m, d, z_y, sum z) of a block of logits, base-2 as the library
+    defines them (test-side restatement; numpy float64)."""
+    import numpy as np
+    t = z * np.log2(np.e)
+    m = t.max(axis=1)
+    d = np.exp2(t - m[:, None]).sum(axis=1)
+    return m, d
+
+
+def _protocol_worker(rank, world, port, q):
+    import numpy as np
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
+        from oracle import flce_oracle as O
+        r = np.random.default_rng(5)
+        z = r.standard_normal((6, 10)) * 3.0          # the whole-vocabulary logits
+        y = np.array([0, 9, 4, 6, 2, 7])
+        cuts = [0, 3, 10]                               # uneven shards of V = 10
+        a, b = cuts[rank], cuts[rank + 1]
+        zl = z[:, a:b]
+        m, d = _stats_of(zl)
+        inside = (y >= a) & (y < b)
+        zy = np.where(inside, z[np.arange(6), y], 0.0)
+        stats = torch.tensor(np.stack([m, d, zy, zl.sum(1)]), dtype=torch.float64)
+
+        def cpu_rescale(s, gmax):  # the kernel's arithmetic, restated for the test
+            s[1] *= torch.exp2(s[0] - gmax)
+            s[0] = gmax
+
+        def gloo_allreduce(t, op):
+            dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+
+        VP.merge_stats(stats, gloo_allreduce, cpu_rescale)
+        lse = (stats[0] + torch.log2(stats[1])) * np.log(2.0)
+        q.put((rank, lse.numpy(), stats[2].numpy(), stats[3].numpy(),
+               O.logsumexp_rows(z), z[np.arange(6), y], z.sum(1)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_vocab_parallel_exchange_protocol_two_ranks():
+    import numpy as np
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_protocol_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    for _ in range(world):
+        rank, lse, zy, sz, ref_lse, ref_zy, ref_sz = q.get(timeout=10)
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-13)
+        np.testing.assert_allclose(zy, ref_zy, rtol=1e-15)
+        np.testing.assert_allclose(sz, ref_sz, rtol=1e-13)
