@@ -249,6 +249,14 @@ flce_status_t flce_forward_noalloc(const flce_params_t* p, const void* x, const 
                                    const void* b, const int64_t* y, float* loss, float* lse,
                                    int32_t* dev_err, void* stream);
 
+/* Failure-detection self-test: launches one kernel that waits, through the
+ * same bounded mbarrier wait the GEMM pipelines use, on a barrier nothing
+ * arrives on. After limit_cycles (1 .. 2^32 SM clock cycles) the wait gives
+ * up and ORs FLCE_DEVERR_TIMEOUT into *dev_err; the kernel returns normally,
+ * so flce_read_device_error then reports FLCE_ERR_TIMEOUT and the CUDA
+ * context stays usable. (The pipelines' own limit is about one second.) */
+flce_status_t flce_selftest_wait_timeout(int32_t* dev_err, int64_t limit_cycles, void* stream);
+
 /* Synchronises `stream`, reads the device error word into *host_err (HOST
  * pointer, may be NULL), clears the device word and maps it to a status:
  * FLCE_OK, FLCE_ERR_TARGET_OUT_OF_RANGE or FLCE_ERR_TIMEOUT. */

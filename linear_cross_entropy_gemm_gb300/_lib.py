@@ -108,6 +108,8 @@ def load() -> ctypes.CDLL:
     lib.flce_backward_shard.restype = ctypes.c_int
     lib.flce_cast_f32.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int32, vp]
     lib.flce_cast_f32.restype = ctypes.c_int
+    lib.flce_selftest_wait_timeout.argtypes = [vp, ctypes.c_int64, vp]
+    lib.flce_selftest_wait_timeout.restype = ctypes.c_int
     lib.flce_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.flce_read_device_error.restype = ctypes.c_int
     lib.flce_status_string.argtypes = [ctypes.c_int]

@@ -30,7 +30,12 @@ using namespace flce;
 
 namespace {
 
-constexpr int64_t kDefaultVocabBlock = 16384;
+// Default backward vocabulary block: the widest multiple of 256 whose staged
+// dL block [N, BVc] fits kDlBudgetBytes (fewer, larger dW / dx GEMMs: less
+// wave-quantisation tail and fewer fp32 dx read-modify-writes), at least
+// kMinVocabBlock.
+constexpr int64_t kDlBudgetBytes = 1LL << 30;
+constexpr int64_t kMinVocabBlock = 4096;
 constexpr size_t kAlign = 256;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -161,10 +166,16 @@ size_t carve_fwd(const flce_params_t* p, void* base, FwdWs* w) {
 }
 
 int64_t vocab_block(const flce_params_t* p) {
-  int64_t bv = p->bwd_vocab_block > 0 ? p->bwd_vocab_block : kDefaultVocabBlock;
+  int64_t bv = p->bwd_vocab_block;
+  if (bv <= 0) {
+    const int64_t n = p->N > 0 ? p->N : 1;
+    bv = kDlBudgetBytes / (n * 2) / 256 * 256;
+    if (bv < kMinVocabBlock) bv = kMinVocabBlock;
+  }
   const int64_t vr = (p->V + 255) / 256 * 256;
   return bv < vr ? bv : vr;
 }
+
 
 struct BwdWs {
   float4* coef;
@@ -716,6 +727,17 @@ flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_
   if (!aligned16(src) || !aligned16(dst)) return FLCE_ERR_ALIGNMENT;
   return launch_cast16(src, static_cast<uint16_t*>(dst), n, dst_fp16 != 0,
                        static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? FLCE_OK
+             : FLCE_ERR_CUDA;
+}
+
+flce_status_t flce_selftest_wait_timeout(int32_t* dev_err, int64_t limit_cycles, void* stream) {
+  if (!dev_err || limit_cycles <= 0 || limit_cycles > (1LL << 32)) return FLCE_ERR_INVALID_ARG;
+  int sms = 0;
+  flce_status_t st = device_info(&sms);
+  if (st != FLCE_OK) return st;
+  return launch_wait_timeout_selftest(reinterpret_cast<int*>(dev_err), limit_cycles,
+                                      static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? FLCE_OK
              : FLCE_ERR_CUDA;
 }

@@ -108,6 +108,8 @@ cudaError_t launch_shard_stats(const ShardStatsArgs& a, cudaStream_t st);
 cudaError_t launch_shard_rescale(float* stats, const float* gmax, int N, cudaStream_t st);
 cudaError_t launch_cast16(const float* src, uint16_t* dst, int64_t n, bool fp16, cudaStream_t st);
 
+cudaError_t launch_wait_timeout_selftest(int* dev_err, long long limit, cudaStream_t st);
+
 cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, int Vb, void* db,
                                bool db_fp32, bool fp16, cudaStream_t st);
 

@@ -338,4 +338,25 @@ cudaError_t launch_cast16(const float* src, uint16_t* dst, int64_t n, bool fp16,
   return cudaGetLastError();
 }
 
+// Failure-detection self-test: one thread waits, through the same bounded
+// mbar_wait the GEMM pipelines use, on an mbarrier that nothing arrives on.
+// The wait gives up after `limit` cycles and sets the timeout bit in dev_err;
+// the kernel then returns normally and the context stays usable.
+__global__ void wait_timeout_selftest_kernel(int* dev_err, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, dev_err, limit);
+}
+
+cudaError_t launch_wait_timeout_selftest(int* dev_err, long long limit, cudaStream_t st) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, st>>>(dev_err, limit);
+  return cudaGetLastError();
+}
+
 }  // namespace flce

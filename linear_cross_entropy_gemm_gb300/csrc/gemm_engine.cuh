@@ -47,6 +47,7 @@ struct GemmGeom {
   int raster_m_inner;     // 1: consecutive tiles advance along M first
   int group;              // >0: tiles walk M inner inside groups of `group` N-tiles
   int ab_fp16;            // operands are fp16 (else bf16)
+  int a_l2, b_l2;         // L2 policy of the A / B loads: 0 normal, 1 evict_last, 2 evict_first
 };
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, int& tn) {
@@ -126,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
-      const uint64_t pol = l2_policy_evict_normal();
+      const uint64_t pol_a = l2_policy(g.a_l2), pol_b = l2_policy(g.b_l2);
       int s = 0;
       uint32_t ph = 0;
       long long issued = 0;
@@ -145,20 +146,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* b = sB + s * kBStageBytes;
           const int k0 = kb * kBK;
           if constexpr (!kAMN) {
-            tma_load_2d(a, &mapA, &full[s], k0 + g.a_k_off, m0 + g.a_mn_off, pol);
+            tma_load_2d(a, &mapA, &full[s], k0 + g.a_k_off, m0 + g.a_mn_off, pol_a);
           } else {
 #pragma unroll
             for (int j = 0; j < kBM / 64; ++j)
               tma_load_2d(a + j * kMnBoxBytes, &mapA, &full[s], m0 + g.a_mn_off + j * 64,
-                          k0 + g.a_k_off, pol);
+                          k0 + g.a_k_off, pol_a);
           }
           if constexpr (!kBMN) {
-            tma_load_2d(b, &mapB, &full[s], k0 + g.b_k_off, n0 + g.b_mn_off, pol);
+            tma_load_2d(b, &mapB, &full[s], k0 + g.b_k_off, n0 + g.b_mn_off, pol_b);
           } else {
 #pragma unroll
             for (int j = 0; j < kBN / 64; ++j)
               tma_load_2d(b + j * kMnBoxBytes, &mapB, &full[s], n0 + g.b_mn_off + j * 64,
-                          k0 + g.b_k_off, pol);
+                          k0 + g.b_k_off, pol_b);
           }
           ++issued;
           if (++s == kStages) {
@@ -321,7 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------- TMA producer (both CTAs)
-      const uint64_t pol = l2_policy_evict_normal();
+      const uint64_t pol_a = l2_policy(g.a_l2), pol_b = l2_policy(g.b_l2);
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       int s = 0;
       uint32_t ph = 0;
@@ -344,20 +345,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* b = sB + s * kPairBStageBytes;
           const int k0 = kb * kBK;
           if constexpr (!kAMN) {
-            tma_load_2d_pair(a, &mapA, fb, k0 + g.a_k_off, m0 + g.a_mn_off, pol);
+            tma_load_2d_pair(a, &mapA, fb, k0 + g.a_k_off, m0 + g.a_mn_off, pol_a);
           } else {
 #pragma unroll
             for (int j = 0; j < kBM / 64; ++j)
               tma_load_2d_pair(a + j * kMnBoxBytes, &mapA, fb, m0 + g.a_mn_off + j * 64,
-                               k0 + g.a_k_off, pol);
+                               k0 + g.a_k_off, pol_a);
           }
           if constexpr (!kBMN) {
-            tma_load_2d_pair(b, &mapB, fb, k0 + g.b_k_off, n0 + g.b_mn_off, pol);
+            tma_load_2d_pair(b, &mapB, fb, k0 + g.b_k_off, n0 + g.b_mn_off, pol_b);
           } else {
 #pragma unroll
             for (int j = 0; j < (kBN / 2) / 64; ++j)
               tma_load_2d_pair(b + j * kMnBoxBytes, &mapB, fb, n0 + g.b_mn_off + j * 64,
-                               k0 + g.b_k_off, pol);
+                               k0 + g.b_k_off, pol_b);
           }
           ++issued;
           if (++s == kPairStages) {

@@ -49,15 +49,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits until the phase with the given parity has completed. Returns false
-// (and leaves the abort flag set) if this or another role gave up.
+// (and leaves the abort flag set) if this or another role gave up, or after
+// `limit` clock cycles without progress.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* dev_err) {
+                                          int* dev_err, long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       if (dev_err) atomicOr(dev_err, kDevErrTimeout);
       return false;
@@ -91,6 +92,16 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 0 = normal, 1 = evict_last (operand reused by many tiles), 2 = evict_first (streamed).
+__device__ __forceinline__ uint64_t l2_policy(int kind) {
+  return kind == 1 ? l2_policy_evict_last() : kind == 2 ? l2_policy_evict_first()
+                                                        : l2_policy_evict_normal();
 }
 
 // ----------------------------------------------------------------- tcgen05

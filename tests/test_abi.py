@@ -97,3 +97,19 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(ImportError):
         _lib.load()
+
+
+@pytest.mark.parametrize("lang,std", [("c", "-std=c99"), ("c++", "-std=c++17")])
+def test_header_compiles_as_plain_c_and_cpp(tmp_path, lang, std):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") if lang == "c" else shutil.which("g++")
+    if cc is None:
+        pytest.skip("no host compiler")
+    calls = "\n".join(f"  (void)&{n};" for n in declared_functions())
+    src = tmp_path / ("use." + ("c" if lang == "c" else "cpp"))
+    src.write_text('#include "flce.h"\nint main(void) {\n  flce_params_t p = {0};\n'
+                   '  (void)p;\n' + calls + "\n  return 0;\n}\n")
+    r = subprocess.run([cc, std, "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
