@@ -39,12 +39,12 @@ WORKLOAD = "llama3_head"
 METRIC = "FLCE fwd+bwd ms, tokens/s, TFLOP/s (% bf16 TC peak) @ 8192×4096×128256"
 PAGES_MS = 19.897  # Liger-Kernel commit 95b01e9, B200, same shape (context)
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of each CTA-pair
-# GEMM from one ncu capture (profiles/gemm_cta_pair_fwd_dw_dx_8192x4096x32768.md):
-# the backward launches there have this workload's per-launch shape (one
-# 16384-column vocabulary block); the forward's is scaled by V (128256/32768).
-# Must be re-measured (or removed) whenever one of these kernels changes.
-TRAFFIC_PER_LAUNCH = {"bwd_dw": 1.466e9, "bwd_dx": 1.373e9, "fwd_lse": 1.342e9 * 128256 / 32768}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch (average over the
+# step's launches of that kernel) from one ncu capture of this workload's full
+# step (1-pass metrics; profiles/dram_traffic_llama3_head.md). Must be
+# re-measured (or removed) whenever one of these kernels or its raster changes.
+TRAFFIC_PER_LAUNCH = {"fwd_lse": 2.362e9, "bwd_dlogits": 2.529e9, "bwd_dw": 7.060e9,
+                      "bwd_dx": 6.668e9}
 
 
 def peaks():
@@ -335,7 +335,9 @@ def run_ours(args):
                 "ms_per_step": dom_ms_per_step,
                 "algorithmic_flops_per_step": flops_per[dom],
                 "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
-                            and os.environ.get("FLCE_CTA_PAIR", "1") != "0" else None),
+                            and not args.bwd_vocab_block
+                            and os.environ.get("FLCE_CTA_PAIR", "1") != "0"
+                            and os.environ.get("FLCE_RASTER", "1") != "0" else None),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm"],

@@ -230,6 +230,15 @@ GemmGeom geom(int M, int N, int K, bool fp16) {
   return g;
 }
 
+// Tile order. FLCE_RASTER=0 selects the plain orders (M inner for the
+// logits GEMMs, N inner for dW / dx); the default bands the reused operand so
+// its slice stays in L2 (bands of 16 pair-M-tiles = 4096 tokens of x for the
+// logits GEMMs, 8 N-tiles = 2048 columns of x for dW).
+bool use_bands() {
+  const char* e = std::getenv("FLCE_RASTER");
+  return !(e && e[0] == '0');
+}
+
 int grid_for(const GemmGeom& g, int sms) {
   const int tiles = g.tiles_m * g.tiles_n;
   return tiles < sms ? tiles : sms;
@@ -370,6 +379,7 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   if (!tr.begin()) return FLCE_ERR_CUDA;
   const bool f16 = p->input_fp16 != 0;
   GemmGeom g = geom(N, V, H, f16);
+  if (use_bands()) g.band_m = pair ? 16 : 32;
   FwdLseArgs ea;
   ea.bias = static_cast<const uint16_t*>(p->has_bias ? b : nullptr);
   ea.fp16 = f16 ? 1 : 0;
@@ -579,6 +589,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     }
     GemmGeom g1 = geom(N, Vb, H, f16);
     g1.b_mn_off = v0;
+    if (use_bands()) g1.band_m = pair ? 16 : 32;
     DlogitsArgs da;
     da.bias = static_cast<const uint16_t*>(p->has_bias ? b : nullptr);
     da.fp16 = p->input_fp16;
@@ -611,6 +622,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     // dW block: one GEMM over all tokens (M = vocab rows, K = tokens).
     GemmGeom g2 = geom(Vb, H, N, f16);
     g2.raster_m_inner = 0;
+    if (use_bands()) g2.band_n = 8;
     DwArgs wa;
     wa.out = dW;
     wa.out_bf16 = p->dW_fp32 ? 0 : 1;

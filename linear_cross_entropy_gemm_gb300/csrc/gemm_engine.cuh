@@ -46,12 +46,31 @@ struct GemmGeom {
   int b_mn_off, b_k_off;
   int raster_m_inner;     // 1: consecutive tiles advance along M first
   int group;              // >0: tiles walk M inner inside groups of `group` N-tiles
+  int band_m;             // >0: bands of band_m M-tiles; inside a band M inner, N outer
+  int band_n;             // >0: bands of band_n N-tiles; inside a band N inner, M outer
   int ab_fp16;            // operands are fp16 (else bf16)
   int a_l2, b_l2;         // L2 policy of the A / B loads: 0 normal, 1 evict_last, 2 evict_first
 };
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, int& tn) {
-  if (g.group > 0) {
+  if (g.band_m > 0) {
+    // A band of band_m M-tiles sweeps every N-tile: its A rows stay in L2 while
+    // the B operand streams; B is read once per band.
+    const int per = g.band_m * g.tiles_n;
+    const int b = t / per;
+    const int r = t - b * per;
+    const int height = min(g.band_m, g.tiles_m - b * g.band_m);
+    tn = r / height;
+    tm = b * g.band_m + (r - tn * height);
+  } else if (g.band_n > 0) {
+    // A band of band_n N-tiles sweeps every M-tile: its B columns stay in L2.
+    const int per = g.band_n * g.tiles_m;
+    const int b = t / per;
+    const int r = t - b * per;
+    const int width = min(g.band_n, g.tiles_n - b * g.band_n);
+    tm = r / width;
+    tn = b * g.band_n + (r - tm * width);
+  } else if (g.group > 0) {
     // Grouped raster: within a band of `group` N-tiles, walk M first.
     const int band = g.group * g.tiles_m;
     const int b = t / band;
