@@ -163,7 +163,10 @@ def run_reference(args):
         return
     from linear_cross_entropy_gemm_gb300 import inputs as I
     wl = I.WORKLOADS[WORKLOAD]
-    rows = args.ref_rows
+    if args.shape:
+        n_, h_, v_ = (int(t) for t in args.shape.split(","))
+        wl = wl.with_(name=f"{wl.name}-shape", N=n_, H=h_, V=v_)
+    rows = min(args.ref_rows, wl.N)
     sample = OracleSample(wl, rows)
     for _ in range(min(args.warmup, 1)):
         sample.run()

@@ -284,7 +284,9 @@ struct DlogitsEpi {
       }
       if constexpr (HAS_BIAS) {
         const float colsum = warp_column_sums(v, lane);
-        if (colb0 + lane < a.Vb)
+        // A CTA pair's second half-tile can lie wholly past the last token
+        // (odd count of 128-row tiles): it has no partial row of its own.
+        if (colb0 + lane < a.Vb && tm * kBM < a.Ntok)
           a.db_part[static_cast<size_t>(tm * 4 + quad) * a.ld_db + colb0 + lane] = colsum;
       }
     }

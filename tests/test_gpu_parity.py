@@ -83,6 +83,14 @@ def test_bf16_gradients_and_custom_ignore_index(store):
                store=store)
 
 
+@pytest.mark.parametrize("store", MODES)
+def test_negative_logit_scale_and_class_zero_ignored(store):
+    wl = I.Workload("negscale", N=257, H=136, V=999, seed=33, b_std=0.2, ignore_frac=0.0,
+                    ignore_index=0, logit_scale=-0.75, label_smoothing=0.05,
+                    lse_square_scale=2e-3, reduction="mean")
+    full_check(wl, bwd_vocab_block=512, store=store)
+
+
 def test_large_logits_small_shape_both_modes():
     # logit std ~45 (x, W, b ~ N(0, 1)): most tile probabilities underflow fp16
     # in the stored mode; the ones that matter must survive.
@@ -285,3 +293,56 @@ def test_non_contiguous_inputs_are_rejected():
     y = torch.zeros(64, dtype=torch.int64, device=dev)
     with pytest.raises(ValueError):
         F.flce_forward(x, W, None, y)
+
+
+@pytest.mark.parametrize("store", MODES)
+@pytest.mark.parametrize("N", [300, 129, 1])
+def test_no_writes_outside_caller_buffers(N, store):
+    # Every buffer the library writes gets a canary-filled guard region after
+    # it (N = 300: an odd number of 128-row tiles, so a CTA pair's second half
+    # is pure padding); the guards must be untouched after forward + backward.
+    wl = I.Workload("guard", N=N, H=136, V=1300, seed=34, b_std=0.1, ignore_frac=0.1,
+                    label_smoothing=0.1, lse_square_scale=1e-3)
+    inp = I.make_inputs(wl)
+    p = DeviceProblem(inp)
+    opts = opts_of(wl)
+    dev = p.dev
+    G = 1 << 16  # guard bytes
+
+    def guarded(nbytes):
+        t = torch.full((nbytes + G,), 0xA5, dtype=torch.uint8, device=dev)
+        return t
+
+    def check(t, nbytes, what):
+        tail = t[nbytes:]
+        assert bool((tail == 0xA5).all()), f"{what}: write past the end"
+
+    nf = F.flce_workspace_size(N, wl.H, wl.V, "forward", **opts)
+    nb = F.flce_workspace_size(N, wl.H, wl.V, "backward", bwd_vocab_block=512, **opts)
+    wf, wb = guarded(nf), guarded(nb)
+    saved = None
+    ns = 0
+    if store:
+        ns = F.flce_saved_size(N, wl.H, wl.V, **opts)
+        saved = guarded(ns)
+    lossb, lseb = guarded(4), guarded(4 * N)
+    dxb, dWb, dbb = guarded(2 * N * wl.H), guarded(4 * wl.V * wl.H), guarded(4 * wl.V)
+    loss = lossb[:4].view(torch.float32)
+    lse = lseb[:4 * N].view(torch.float32)
+    dx = dxb[:2 * N * wl.H].view(torch.bfloat16).view(N, wl.H)
+    dW = dWb[:4 * wl.V * wl.H].view(torch.float32).view(wl.V, wl.H)
+    db = dbb[:4 * wl.V].view(torch.float32)
+    F.flce_forward(p.x, p.W, p.b, p.y, workspace=wf[:nf], out=(loss, lse),
+                   saved=None if saved is None else saved[:ns], **opts)
+    F.flce_backward(p.dloss, lse, p.x, p.W, p.b, p.y, workspace=wb[:nb], out=(dx, dW, db),
+                    bwd_vocab_block=512, saved=None if saved is None else saved[:ns], **opts)
+    torch.cuda.synchronize()
+    assert F.flce_read_device_error(dev) == 0
+    for t, n, what in ((wf, nf, "forward workspace"), (wb, nb, "backward workspace"),
+                       (lossb, 4, "loss"), (lseb, 4 * N, "lse"), (dxb, 2 * N * wl.H, "dx"),
+                       (dWb, 4 * wl.V * wl.H, "dW"), (dbb, 4 * wl.V, "db")):
+        check(t, n, what)
+    if store:
+        check(saved, ns, "saved state")
+    ref = p.run(bwd_vocab_block=512, store=store)
+    assert torch.equal(ref["dW"], dW) and torch.equal(ref["db"], db)
