@@ -279,26 +279,36 @@ def run_ours(args):
     if not args.no_stored_mode:
         saved = torch.empty(F.flce_saved_size(N, H, V, **opts), dtype=torch.uint8, device=dev)
 
-        def step_stored():
-            F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), saved=saved, **opts)
+        def step_stored(trace=False):
+            F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), saved=saved,
+                           trace=ftr if trace else None, **opts)
             F.flce_backward(dloss, lse, x, W, None, y, workspace=bws, out=(dx, dW, None),
-                            saved=saved, bwd_vocab_block=bvb, **opts)
+                            saved=saved, bwd_vocab_block=bvb, trace=btr if trace else None,
+                            **opts)
 
         for _ in range(args.warmup):
             step_stored()
         barrier()
         sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+        sk = {}
         for i in range(args.steps):
             flush.zero_()
             sev[i][0].record(stream)
-            step_stored()
+            step_stored(trace=True)
             sev[i][1].record(stream)
+            torch.cuda.synchronize(dev)
+            for name, kms in ftr.launches() + btr.launches():
+                sk.setdefault(name, []).append(kms)
         barrier()
         sms = max_over_ranks(sum(a.elapsed_time(b) for a, b in sev) / args.steps, ws, dev)
         stored = {"ms_per_step": sms, "value": ws * N / (sms * 1e-3), "unit": "tokens/s",
                   "tflops_6nhv": 6.0 * N * H * V / (sms * 1e-3) / 1e12,
                   "saved_bytes": saved.numel(),
+                  "kernels": {("bwd_convert" if k == "bwd_dlogits" else
+                               "fwd_lse_store" if k == "fwd_lse" else k):
+                              {"launches_per_step": len(v) // args.steps,
+                               "ms_per_step": sum(v) / args.steps} for k, v in sorted(sk.items())},
                   "note": "flce_forward_store/flce_backward_store: fp16 tile probabilities "
                           "kept from the forward, no logits recompute (6NHV flops)"}
         del saved
