@@ -21,6 +21,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/flce.h"
 #include "epilogues.cuh"
@@ -244,6 +245,15 @@ int grid_for(const GemmGeom& g, int sms) {
   return tiles < sms ? tiles : sms;
 }
 
+// NVTX range over a scope (host timeline; free unless a profiler is attached),
+// so Nsight Systems shows each call and each backward vocabulary block.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // Records the caller's events around each launch (flce_trace_t in flce.h).
 struct Tracer {
   flce_trace_t* t;
@@ -333,6 +343,9 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
                                   void* saved, size_t saved_bytes, void* workspace,
                                   size_t workspace_bytes, int32_t* dev_err, void* stream,
                                   flce_trace_t* trace, float* shard_stats) {
+  NvtxRange nvtx_range(shard_stats ? "flce_forward_shard"
+                       : saved     ? "flce_forward_store"
+                                   : "flce_forward");
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
   if (shard_stats) {
@@ -491,6 +504,9 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
                                    void* dW, void* db, void* workspace, size_t workspace_bytes,
                                    int32_t* dev_err, void* stream, flce_trace_t* trace,
                                    bool shard) {
+  NvtxRange nvtx_range(shard   ? "flce_backward_shard"
+                       : saved ? "flce_backward_store"
+                               : "flce_backward");
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
   if (shard ? p->vocab_total == 0 : !whole_vocab(p)) return FLCE_ERR_INVALID_ARG;
@@ -556,6 +572,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     return FLCE_ERR_CUDA;
 
   for (int blk = 0; blk < nblk; ++blk) {
+    NvtxRange nvtx_block("flce_backward_vocab_block");
     const int v0 = static_cast<int>(blk * bv);
     const int Vb = static_cast<int>(V - v0 < bv ? V - v0 : bv);
     CUtensorMap mdl_k, mdl_mn;
