@@ -204,15 +204,21 @@ cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, 
 // Stored-probability backward: dL[n, v] = a_n q[n, v] 2^(m_t(n) - lse2_n)
 //   - c_n - t_n [v == y_n] for the vocab block [v0, v0 + Vb), q being the
 // forward's fp16 2^(z log2e - m_t). One CTA covers 32 tokens x one 256-column
-// vocab tile (one m_t per token); thread i owns columns 2i, 2i + 1 and also
-// writes their fp32 column sums over the 32 tokens (db partials, row blockIdx.y).
+// vocab tile (one m_t per token). Thread i owns 8 columns (16-byte loads and
+// stores) of rows i/32, i/32 + 4, ..., so eight independent loads are in
+// flight per thread; the fp32 column sums over the 32 tokens (db partials,
+// row blockIdx.y) are combined through shared memory.
 constexpr int kConvRows = 32;
+constexpr int kConvRowGroups = 4;  // 128 threads = 32 column groups x 4 row groups
 __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs a) {
   __shared__ float s_scale[kConvRows], s_c[kConvRows], s_t[kConvRows];
   __shared__ int s_ty[kConvRows];
-  const int tile = blockIdx.x;                  // 256-column tile inside the block
+  __shared__ float s_sum[kConvRowGroups][256];
+  const int tile = blockIdx.x;  // 256-column tile inside the block
   const int r0 = blockIdx.y * kConvRows;
-  const int colb = tile * 256 + threadIdx.x * 2;  // block-relative column
+  const int cg = threadIdx.x & 31;
+  const int rg = threadIdx.x >> 5;
+  const int colb = tile * 256 + cg * 8;  // block-relative first column of this thread
   if (threadIdx.x < kConvRows) {
     const int r = r0 + threadIdx.x;
     float sc = 0.f, c = 0.f, t = 0.f;
@@ -233,27 +239,55 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
     s_ty[threadIdx.x] = ty;
   }
   __syncthreads();
-  const bool ok0 = colb < a.Vb, ok1 = colb + 1 < a.Vb;
   const float dls = a.dl_scale[0];
-  float sum0 = 0.f, sum1 = 0.f;
-  const int rows = min(kConvRows, a.N - r0);
-  for (int i = 0; i < rows; ++i) {
-    const size_t r = static_cast<size_t>(r0 + i);
-    const __half2 q = *reinterpret_cast<const __half2*>(a.probs + r * a.ld_p + a.v0 + colb);
-    const float2 qf = __half22float2(q);
-    float d0 = fmaf(s_scale[i], qf.x, -s_c[i]) - (colb == s_ty[i] ? s_t[i] : 0.f);
-    float d1 = fmaf(s_scale[i], qf.y, -s_c[i]) - (colb + 1 == s_ty[i] ? s_t[i] : 0.f);
-    d0 = ok0 ? d0 : 0.f;
-    d1 = ok1 ? d1 : 0.f;
-    sum0 += d0;
-    sum1 += d1;
-    *reinterpret_cast<uint32_t*>(a.dL + r * a.ld_dL + colb) =
-        pack_16x2(d0 * dls, d1 * dls, a.fp16 != 0);
+  const bool f16 = a.fp16 != 0;
+  float sum[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sum[j] = 0.f;
+  uint4 q[kConvRows / kConvRowGroups];
+#pragma unroll
+  for (int k = 0; k < kConvRows / kConvRowGroups; ++k) {
+    const int i = rg + kConvRowGroups * k;
+    if (r0 + i < a.N)
+      q[k] = __ldg(reinterpret_cast<const uint4*>(
+          a.probs + static_cast<size_t>(r0 + i) * a.ld_p + a.v0 + colb));
+  }
+#pragma unroll
+  for (int k = 0; k < kConvRows / kConvRowGroups; ++k) {
+    const int i = rg + kConvRowGroups * k;
+    if (r0 + i >= a.N) continue;
+    const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+    float d[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+      d[2 * e] = f.x;
+      d[2 * e + 1] = f.y;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      float v = fmaf(s_scale[i], d[j], -s_c[i]) - (colb + j == s_ty[i] ? s_t[i] : 0.f);
+      v = colb + j < a.Vb ? v : 0.f;
+      sum[j] += v;
+      d[j] = v * dls;
+    }
+    uint4 o;
+    o.x = pack_16x2(d[0], d[1], f16);
+    o.y = pack_16x2(d[2], d[3], f16);
+    o.z = pack_16x2(d[4], d[5], f16);
+    o.w = pack_16x2(d[6], d[7], f16);
+    *reinterpret_cast<uint4*>(a.dL + static_cast<size_t>(r0 + i) * a.ld_dL + colb) = o;
   }
   if (a.db_part) {
-    float* dp = a.db_part + static_cast<size_t>(blockIdx.y) * a.ld_db + colb;
-    if (ok0) dp[0] = sum0;
-    if (ok1) dp[1] = sum1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s_sum[rg][cg * 8 + j] = sum[j];
+    __syncthreads();
+    // Fixed order over the four row groups: deterministic.
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) {
+      const float tot = ((s_sum[0][c] + s_sum[1][c]) + s_sum[2][c]) + s_sum[3][c];
+      if (tile * 256 + c < a.Vb)
+        a.db_part[static_cast<size_t>(blockIdx.y) * a.ld_db + tile * 256 + c] = tot;
+    }
   }
 }
 
