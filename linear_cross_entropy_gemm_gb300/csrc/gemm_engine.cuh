@@ -45,11 +45,9 @@ struct GemmGeom {
   int a_mn_off, a_k_off;  // added to the A / B load coordinates
   int b_mn_off, b_k_off;
   int raster_m_inner;     // 1: consecutive tiles advance along M first
-  int group;              // >0: tiles walk M inner inside groups of `group` N-tiles
   int band_m;             // >0: bands of band_m M-tiles; inside a band M inner, N outer
   int band_n;             // >0: bands of band_n N-tiles; inside a band N inner, M outer
   int ab_fp16;            // operands are fp16 (else bf16)
-  int a_l2, b_l2;         // L2 policy of the A / B loads: 0 normal, 1 evict_last, 2 evict_first
 };
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, int& tn) {
@@ -70,14 +68,6 @@ __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, i
     const int width = min(g.band_n, g.tiles_n - b * g.band_n);
     tm = r / width;
     tn = b * g.band_n + (r - tm * width);
-  } else if (g.group > 0) {
-    // Grouped raster: within a band of `group` N-tiles, walk M first.
-    const int band = g.group * g.tiles_m;
-    const int b = t / band;
-    const int r = t - b * band;
-    const int width = min(g.group, g.tiles_n - b * g.group);
-    tm = r / width;
-    tn = b * g.group + (r - tm * width);
   } else if (g.raster_m_inner) {
     tm = t % g.tiles_m;
     tn = t / g.tiles_m;
@@ -146,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
-      const uint64_t pol_a = l2_policy(g.a_l2), pol_b = l2_policy(g.b_l2);
+      const uint64_t pol_a = l2_policy_evict_normal(), pol_b = pol_a;
       int s = 0;
       uint32_t ph = 0;
       long long issued = 0;
@@ -341,7 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------- TMA producer (both CTAs)
-      const uint64_t pol_a = l2_policy(g.a_l2), pol_b = l2_policy(g.b_l2);
+      const uint64_t pol_a = l2_policy_evict_normal(), pol_b = pol_a;
       const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
       int s = 0;
       uint32_t ph = 0;

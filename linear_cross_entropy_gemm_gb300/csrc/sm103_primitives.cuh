@@ -82,28 +82,13 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 
-// L2 eviction-priority policies for cache hints (createpolicy fractional).
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
+// L2 cache-hint policy for the TMA loads (normal eviction priority; the
+// evict_first / evict_last variants were measured and raised DRAM traffic).
 __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-// 0 = normal, 1 = evict_last (operand reused by many tiles), 2 = evict_first (streamed).
-__device__ __forceinline__ uint64_t l2_policy(int kind) {
-  return kind == 1 ? l2_policy_evict_last() : kind == 2 ? l2_policy_evict_first()
-                                                        : l2_policy_evict_normal();
-}
-
 // ----------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

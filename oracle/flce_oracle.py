@@ -3,7 +3,8 @@
 TEST INFRASTRUCTURE. Only the tests, the smoke check and the benchmark's CPU
 baseline may import this module. The library never does, and shares no code
 with it: this file restates the mathematics of the pages in plain numpy,
-float64, over the same bf16-rounded inputs the GPU sees (widened exactly).
+float64, over the same bf16- (or fp16-) rounded inputs the GPU sees, widened
+exactly; also pinned against planted mistakes (tests/test_oracle_mutants.py).
 
 What it computes (the plain definition; the GPU path reaches the same result
 up to rounding order, by tiling and online softmax):

@@ -1,0 +1,49 @@
+"""Seeded randomized parity sweep: small random shapes (N, H, V off the tile
+grid, including single rows / columns), random loss options, bias, operand
+type, backward mode and vocabulary block, each compared element by element
+with the CPU oracle. The case list is fixed by the seed, so failures
+reproduce."""
+import numpy as np
+import pytest
+import torch
+
+from linear_cross_entropy_gemm_gb300 import inputs as I
+
+from test_gpu_parity import full_check
+
+pytestmark = pytest.mark.gpu
+
+
+def _cases(n=24, seed=20261202):
+    r = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        red = ["mean", "sum", "none"][r.integers(3)]
+        V = int(r.choice([1, 2, 255, 256, 257, int(r.integers(3, 3000))]))
+        wl = I.Workload(
+            f"fuzz{i}", N=int(r.choice([1, 2, 127, 128, 129, 255, 257, int(r.integers(1, 700))])),
+            H=int(8 * r.integers(1, 40)), V=V, seed=5000 + i,
+            x_std=float(r.choice([0.5, 1.0, 3.0])), w_std=float(r.choice([0.02, 0.2, 1.0])),
+            b_std=None if r.random() < 0.5 else float(r.choice([0.01, 0.5])),
+            ignore_frac=float(r.choice([0.0, 0.1, 0.5])),
+            ignore_index=int(r.choice([-100, 0, 3])),
+            label_smoothing=float(r.choice([0.0, 0.1, 0.7])),
+            lse_square_scale=float(r.choice([0.0, 1e-4, 1e-2])),
+            logit_scale=float(r.choice([1.0, 0.3, -1.2])), reduction=red,
+            dloss="normal_per_token" if red == "none" else str(r.choice(["one", "normal_scalar"])),
+            dtype=str(r.choice(["bf16", "bf16", "fp16"])))
+        if wl.dtype == "fp16":
+            # fp16 gradients are produced in fp16: as in fp16 training, a loss
+            # scale keeps them above fp16's smallest normal (6.1e-5), where its
+            # subnormal spacing alone would be a percent-level error.
+            wl = wl.with_(dloss_scale=1024.0)
+        bvb = int(r.choice([0, 256, 512, 1024]))
+        store = bool(r.random() < 0.4)
+        out.append(pytest.param(wl, bvb, store, id=f"{wl.name}-N{wl.N}-H{wl.H}-V{wl.V}-{wl.dtype}"
+                                f"-{red}-bv{bvb}-{'st' if store else 'rc'}"))
+    return out
+
+
+@pytest.mark.parametrize("wl,bvb,store", _cases())
+def test_random_shapes_and_options(wl, bvb, store):
+    full_check(wl, bwd_vocab_block=bvb, store=store)
