@@ -221,8 +221,20 @@ def run_ours(args):
                 lse_square_scale=wl.lse_square_scale, logit_scale=wl.logit_scale,
                 reduction=wl.reduction)
     N, H, V = wl.N, wl.H, wl.V
+    from linear_cross_entropy_gemm_gb300 import tuning
+    tune = None
+    fkw, bkw = {}, {"bwd_vocab_block": args.bwd_vocab_block}
+    if args.autotune:
+        res = tuning.autotune(x, W, None, y, dloss=dloss, reps=3, **opts)
+        fkw, bkw = res.config.forward_kwargs(), res.config.backward_kwargs()
+        tune = res.as_dict()
+    bvb = bkw["bwd_vocab_block"]
+    bv_used = bvb or tuning.library_default_block(N, V)
+    env_form = "single" if os.environ.get("FLCE_CTA_PAIR", "1") == "0" else "pair"
+    forms_used = {"forward": fkw.get("gemm_form", "default"), "backward": bkw.get("gemm_form", "default")}
+    forms_used = {k: env_form if f == "default" else f for k, f in forms_used.items()}
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", **opts), dtype=torch.uint8, device=dev)
-    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", bwd_vocab_block=args.bwd_vocab_block,
+    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", bwd_vocab_block=bvb,
                                             **opts), dtype=torch.uint8, device=dev)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
@@ -233,13 +245,11 @@ def run_ours(args):
     ftr, btr = F.KernelTrace(8), F.KernelTrace(256)
     host_loss = torch.empty(1, dtype=torch.float32).pin_memory()
 
-    bvb = args.bwd_vocab_block
-
     def step(trace=False):
         F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), trace=ftr if trace else None,
-                       **opts)
+                       **opts, **fkw)
         F.flce_backward(dloss, lse, x, W, None, y, workspace=bws, out=(dx, dW, None),
-                        trace=btr if trace else None, bwd_vocab_block=bvb, **opts)
+                        trace=btr if trace else None, **opts, **bkw)
 
     def barrier():
         if ws > 1:
@@ -281,10 +291,9 @@ def run_ours(args):
 
         def step_stored(trace=False):
             F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), saved=saved,
-                           trace=ftr if trace else None, **opts)
+                           trace=ftr if trace else None, **opts, **fkw)
             F.flce_backward(dloss, lse, x, W, None, y, workspace=bws, out=(dx, dW, None),
-                            saved=saved, bwd_vocab_block=bvb, trace=btr if trace else None,
-                            **opts)
+                            saved=saved, trace=btr if trace else None, **opts, **bkw)
 
         for _ in range(args.warmup):
             step_stored()
@@ -348,8 +357,8 @@ def run_ours(args):
                 "ms_per_step": dom_ms_per_step,
                 "algorithmic_flops_per_step": flops_per[dom],
                 "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
-                            and not args.bwd_vocab_block
-                            and os.environ.get("FLCE_CTA_PAIR", "1") != "0"
+                            and bv_used == tuning.library_default_block(N, V)
+                            and forms_used == {"forward": "pair", "backward": "pair"}
                             and os.environ.get("FLCE_RASTER", "1") != "0" else None),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
     else:
@@ -368,8 +377,8 @@ def run_ours(args):
         "config": {"workload": f"{wl.name}: N={N} H={H} V={V} bf16, mean, no bias, dloss=1",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "flushed (256 MiB write) before each timed step, outside the events",
-                   "bwd_vocab_block": args.bwd_vocab_block or 16384, "dW_dtype": "fp32",
-                   "gemm": "cta pair" if os.environ.get("FLCE_CTA_PAIR", "1") != "0" else "single cta",
+                   "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
+                   "gemm_form": forms_used,
                    "N": N, "H": H, "V": V},
         "tflops_8nhv": tflops, "frac_bf16_peak_8nhv": tflops / pk["bf16_sus"],
         "tflops_6nhv_useful": tflops * 0.75,
@@ -384,6 +393,8 @@ def run_ours(args):
         "wall_s_timed": wall,
         "stored_mode": stored,
     }
+    if tune is not None:
+        line["autotune"] = tune
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
     if rank == 0:
@@ -403,6 +414,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="N,H,V override (profiling captures only)")
     ap.add_argument("--no-stored-mode", action="store_true")
+    ap.add_argument("--autotune", action="store_true",
+                    help="time the GEMM forms and backward vocabulary blocks first and run the "
+                         "fastest (tuning.autotune); the table goes into the JSON line")
     ap.add_argument("--bwd-vocab-block", type=int, default=0,
                     help="backward vocabulary block (multiple of 256); 0 = library default")
     args = ap.parse_args()

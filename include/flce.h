@@ -66,6 +66,16 @@ typedef enum {
   FLCE_ERR_UNSUPPORTED = 7        /* device is not sm_103 / sizes beyond the int32 tile grid */
 } flce_status_t;
 
+/* GEMM kernel form of a call (flce_params_t.gemm_form). Both forms compute
+ * the same products; results differ only in the order of fp32 accumulation
+ * inside a tile, not in what is summed. */
+typedef enum {
+  FLCE_GEMM_DEFAULT = 0,    /* library default: CTA pairs (FLCE_CTA_PAIR=0 or 1 in the
+                               environment overrides the default, not an explicit form) */
+  FLCE_GEMM_SINGLE_CTA = 1, /* one CTA per 128 x 256 tile (tcgen05 cta_group::1) */
+  FLCE_GEMM_CTA_PAIR = 2    /* two CTAs of a cluster per 256 x 256 tile (cta_group::2) */
+} flce_gemm_form_t;
+
 /* Device error word bits (see flce_read_device_error). */
 #define FLCE_DEVERR_TARGET 1
 #define FLCE_DEVERR_TIMEOUT 2
@@ -88,7 +98,7 @@ typedef struct {
                                vocabulary; the plain calls require 0 or V) */
   int32_t input_fp16;       /* 0: x, W, b are bf16; 1: they are fp16 (dx, and dW / db when
                                not fp32, are then fp16 too) */
-  int32_t reserved;         /* must be 0 */
+  int32_t gemm_form;        /* flce_gemm_form_t; 0 = library default */
 } flce_params_t;
 
 /* Kernel kinds reported by the traced entry points. */

@@ -21,12 +21,13 @@ from typing import Optional, Tuple
 import torch
 
 from . import _lib
-from ._lib import FlceError, params
+from ._lib import GEMM_FORMS, FlceError, params
 
 __all__ = [
     "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
     "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
     "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace", "flce_saved_size",
+    "GEMM_FORMS",
 ]
 
 _err_words = {}
@@ -114,11 +115,14 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
                  reduction: str = "mean", workspace: Optional[torch.Tensor] = None,
                  out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
                  stream=None, trace: Optional[KernelTrace] = None,
-                 saved: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+                 saved: Optional[torch.Tensor] = None,
+                 gemm_form="default") -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss and per-token lse. loss is a 0-dim fp32 tensor (sum/mean) or [N]
     fp32 (none); lse is [N] fp32. Runs on the current stream, no sync.
     With ``saved`` (a uint8 CUDA tensor of flce_saved_size bytes) the forward
-    also keeps the state the stored-probability backward needs."""
+    also keeps the state the stored-probability backward needs.
+    ``gemm_form``: "default", "single" (128 x 256 CTA tiles) or "pair"
+    (256 x 256 tiles on CTA pairs); see ``tuning.autotune``."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
@@ -126,7 +130,7 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     p = params(N, H, V, ignore_index=ignore_index, label_smoothing=label_smoothing,
                lse_square_scale=lse_square_scale, logit_scale=logit_scale,
                reduction=reduction, has_bias=b is not None,
-               input_fp16=x.dtype == torch.float16)
+               input_fp16=x.dtype == torch.float16, gemm_form=gemm_form)
     dev = x.device
     if out is not None:
         loss, lse = out
@@ -158,10 +162,12 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                   dW_dtype: torch.dtype = torch.float32, db_dtype: torch.dtype = torch.float32,
                   bwd_vocab_block: int = 0, workspace: Optional[torch.Tensor] = None,
                   out: Optional[Tuple] = None, stream=None, trace: Optional[KernelTrace] = None,
-                  saved: Optional[torch.Tensor] = None):
+                  saved: Optional[torch.Tensor] = None, gemm_form="default"):
     """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None.
     With ``saved`` (filled by flce_forward(..., saved=)) the logits are not
-    recomputed: dlogits come from the stored tile probabilities."""
+    recomputed: dlogits come from the stored tile probabilities.
+    ``bwd_vocab_block`` (0 = library default) and ``gemm_form`` select the
+    vocabulary block and GEMM form; see ``tuning.autotune``."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
@@ -180,7 +186,8 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                lse_square_scale=lse_square_scale, logit_scale=logit_scale,
                reduction=reduction, has_bias=b is not None,
                dW_fp32=dW_dtype == torch.float32, db_fp32=db_dtype == torch.float32,
-               bwd_vocab_block=bwd_vocab_block, input_fp16=x.dtype == torch.float16)
+               bwd_vocab_block=bwd_vocab_block, input_fp16=x.dtype == torch.float16,
+               gemm_form=gemm_form)
     if out is not None:
         dx, dW, db = out
     else:
@@ -232,17 +239,20 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, x, target, weight, bias=None, ignore_index=-100, label_smoothing=0.0,
-                lse_square_scale=0.0, logit_scale=1.0, reduction="mean", recompute=True):
+                lse_square_scale=0.0, logit_scale=1.0, reduction="mean", recompute=True,
+                config=None):
         saved = None
         if not recompute:
             n = flce_saved_size(x.shape[0], x.shape[1], weight.shape[0],
                                 label_smoothing=label_smoothing,
                                 input_fp16=x.dtype == torch.float16)
             saved = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
+        ctx.config = config
         loss, lse = flce_forward(x, weight, bias, target, ignore_index=ignore_index,
                                  label_smoothing=label_smoothing,
                                  lse_square_scale=lse_square_scale, logit_scale=logit_scale,
-                                 reduction=reduction, saved=saved)
+                                 reduction=reduction, saved=saved,
+                                 **({} if config is None else config.forward_kwargs()))
         ctx.saved_state = saved
         ctx.save_for_backward(x, target, weight, bias, lse)
         ctx.opts = dict(ignore_index=ignore_index, label_smoothing=label_smoothing,
@@ -255,29 +265,35 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
         x, target, weight, bias, lse = ctx.saved_tensors
         dx, dW, db = flce_backward(dloss.float().contiguous(), lse, x, weight, bias, target,
                                    dW_dtype=torch.float32, db_dtype=torch.float32,
-                                   saved=ctx.saved_state, **ctx.opts)
+                                   saved=ctx.saved_state, **ctx.opts,
+                                   **({} if ctx.config is None else ctx.config.backward_kwargs()))
         ctx.saved_state = None
         dW = dW.to(weight.dtype)
         db = None if db is None else db.to(bias.dtype)
-        return dx, None, dW, db, None, None, None, None, None, None
+        return dx, None, dW, db, None, None, None, None, None, None, None
 
 
 def fused_linear_cross_entropy(x, target, weight, bias=None, ignore_index=-100,
                                label_smoothing=0.0, lse_square_scale=0.0, logit_scale=1.0,
-                               reduction="mean", recompute=True):
+                               reduction="mean", recompute=True, config=None):
     """Functional form; x [N, H] bf16, target [N] int64, weight [V, H] bf16.
     recompute=False keeps fp16 tile probabilities (~2 N V bytes) from the
-    forward so the backward skips the logits GEMM."""
+    forward so the backward skips the logits GEMM. ``config``: a
+    ``tuning.FlceConfig`` (GEMM forms, backward vocabulary block), or None for
+    the library defaults."""
     return FusedLinearCrossEntropyFunction.apply(x, target, weight, bias, ignore_index,
                                                  label_smoothing, lse_square_scale,
-                                                 logit_scale, reduction, recompute)
+                                                 logit_scale, reduction, recompute, config)
 
 
 class FusedLinearCrossEntropyLoss(torch.nn.Module):
     """Module form: flattens x [..., H] and target [...] to [N, H] and [N]."""
 
     def __init__(self, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
-                 logit_scale=1.0, reduction="mean", recompute=True):
+                 logit_scale=1.0, reduction="mean", recompute=True, autotune=False):
+        """autotune=True: the first call for each (shape, dtype, options) key
+        times the GEMM forms and backward vocabulary blocks on the caller's
+        tensors (tuning.autotune) and later calls reuse the fastest."""
         super().__init__()
         if reduction not in ("none", "sum", "mean"):
             raise ValueError(f"reduction: {reduction} is not supported")
@@ -287,9 +303,19 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         self.logit_scale = logit_scale
         self.reduction = reduction
         self.recompute = recompute
+        self.autotune = autotune
 
     def forward(self, x, target, weight, bias=None):
+        x2 = x.reshape(-1, x.shape[-1]).contiguous()
+        y2 = target.reshape(-1).contiguous()
+        config = None
+        if self.autotune:
+            from . import tuning
+            config = tuning.autotune(
+                x2.detach(), weight.detach(), None if bias is None else bias.detach(), y2,
+                ignore_index=self.ignore_index, label_smoothing=self.label_smoothing,
+                lse_square_scale=self.lse_square_scale, logit_scale=self.logit_scale,
+                reduction=self.reduction).config
         return fused_linear_cross_entropy(
-            x.reshape(-1, x.shape[-1]).contiguous(), target.reshape(-1).contiguous(), weight,
-            bias, self.ignore_index, self.label_smoothing, self.lse_square_scale,
-            self.logit_scale, self.reduction, self.recompute)
+            x2, y2, weight, bias, self.ignore_index, self.label_smoothing,
+            self.lse_square_scale, self.logit_scale, self.reduction, self.recompute, config)

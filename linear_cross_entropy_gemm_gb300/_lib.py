@@ -18,6 +18,8 @@ STATUS_NAMES = {
     3: "FLCE_ERR_WORKSPACE_TOO_SMALL", 4: "FLCE_ERR_TARGET_OUT_OF_RANGE", 5: "FLCE_ERR_CUDA",
     6: "FLCE_ERR_TIMEOUT", 7: "FLCE_ERR_UNSUPPORTED",
 }
+# flce_gemm_form_t: "default" leaves the choice to the library.
+GEMM_FORMS = {"default": 0, "single": 1, "pair": 2}
 DEVERR_TARGET = 1
 DEVERR_TIMEOUT = 2
 
@@ -40,7 +42,7 @@ class FlceParams(ctypes.Structure):
         ("vocab_start", ctypes.c_int64),
         ("vocab_total", ctypes.c_int64),
         ("input_fp16", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("gemm_form", ctypes.c_int32),
     ]
 
 
@@ -122,11 +124,15 @@ def load() -> ctypes.CDLL:
 
 def params(N, H, V, *, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
            logit_scale=1.0, reduction="mean", has_bias=False, dW_fp32=True, db_fp32=True,
-           bwd_vocab_block=0, vocab_start=0, vocab_total=0, input_fp16=False) -> FlceParams:
+           bwd_vocab_block=0, vocab_start=0, vocab_total=0, input_fp16=False,
+           gemm_form="default") -> FlceParams:
     if reduction not in REDUCTION:
         raise ValueError(f"reduction must be one of {sorted(REDUCTION)}, got {reduction!r}")
+    form = GEMM_FORMS.get(gemm_form, gemm_form) if isinstance(gemm_form, str) else int(gemm_form)
+    if isinstance(form, str):
+        raise ValueError(f"gemm_form must be one of {sorted(GEMM_FORMS)}, got {gemm_form!r}")
     return FlceParams(int(N), int(H), int(V), int(ignore_index), float(label_smoothing),
                       float(lse_square_scale), float(logit_scale), REDUCTION[reduction],
                       int(bool(has_bias)), int(bool(dW_fp32)), int(bool(db_fp32)),
                       int(bwd_vocab_block), int(vocab_start), int(vocab_total),
-                      int(bool(input_fp16)), 0)
+                      int(bool(input_fp16)), form)

@@ -74,9 +74,13 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // GEMM kernel form: CTA pairs (cta_group::2, 256 x 256 tiles) or single CTAs
-// (128 x 256 tiles). FLCE_CTA_PAIR=0 / 1 in the environment overrides the
-// default; both forms compute identical results up to accumulation order.
-bool use_cta_pair() {
+// (128 x 256 tiles). An explicit gemm_form in the parameters decides; with the
+// default form, FLCE_CTA_PAIR=0 / 1 in the environment overrides the library
+// default (pairs). Both forms compute identical results up to accumulation
+// order.
+bool use_cta_pair(const flce_params_t* p) {
+  if (p->gemm_form == FLCE_GEMM_SINGLE_CTA) return false;
+  if (p->gemm_form == FLCE_GEMM_CTA_PAIR) return true;
   const char* e = std::getenv("FLCE_CTA_PAIR");
   if (e && e[0] == '0') return false;
   if (e && e[0] == '1') return true;
@@ -112,7 +116,9 @@ flce_status_t check_params(const flce_params_t* p) {
   if (!(p->logit_scale > -INFINITY && p->logit_scale < INFINITY)) return FLCE_ERR_INVALID_ARG;
   if (p->bwd_vocab_block < 0 || p->bwd_vocab_block % 256 != 0) return FLCE_ERR_INVALID_ARG;
   if (p->has_bias != 0 && p->has_bias != 1) return FLCE_ERR_INVALID_ARG;
-  if ((p->input_fp16 != 0 && p->input_fp16 != 1) || p->reserved != 0) return FLCE_ERR_INVALID_ARG;
+  if (p->input_fp16 != 0 && p->input_fp16 != 1) return FLCE_ERR_INVALID_ARG;
+  if (p->gemm_form < FLCE_GEMM_DEFAULT || p->gemm_form > FLCE_GEMM_CTA_PAIR)
+    return FLCE_ERR_INVALID_ARG;
   if (p->vocab_total == 0) {
     if (p->vocab_start != 0) return FLCE_ERR_INVALID_ARG;
   } else if (p->vocab_total < 0 || p->vocab_total > (1LL << 30) || p->vocab_start < 0 ||
@@ -381,7 +387,7 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   }
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
-  const bool pair = use_cta_pair();
+  const bool pair = use_cta_pair(p);
   CUtensorMap mx, mw;
   if (!encode_2d(&mx, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM, p->input_fp16 != 0) ||
       !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN,
@@ -542,7 +548,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
   const int64_t bv = vocab_block(p);
   const int nblk = cdiv(V, bv);
   int* derr = reinterpret_cast<int*>(dev_err);
-  const bool pair = use_cta_pair();
+  const bool pair = use_cta_pair(p);
 
   Tracer tr{trace, s};
   if (!tr.begin()) return FLCE_ERR_CUDA;

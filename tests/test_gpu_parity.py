@@ -21,10 +21,10 @@ MODES = [pytest.param(False, id="recompute"), pytest.param(True, id="stored")]
 
 
 def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.float32,
-               store=False):
+               store=False, gemm_form="default"):
     inp = I.make_inputs(wl)
     out = DeviceProblem(inp).run(bwd_vocab_block=bwd_vocab_block, dW_dtype=dW_dtype,
-                                 db_dtype=db_dtype, store=store)
+                                 db_dtype=db_dtype, store=store, gemm_form=gemm_form)
     assert out["err"] == 0, f"device error word {out['err']}"
     x64, W64, b64 = f64(inp)
     opts = opts_of(wl)

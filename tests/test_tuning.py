@@ -1,0 +1,72 @@
+"""Host-side logic of the autotuner and the gemm_form parameter (no GPU)."""
+import pytest
+
+from linear_cross_entropy_gemm_gb300 import _lib
+from linear_cross_entropy_gemm_gb300 import build as B
+from linear_cross_entropy_gemm_gb300 import tuning
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return _lib.load()
+
+
+@pytest.mark.parametrize("N,V", [(8192, 128256), (16384, 262144), (512, 4096), (1, 7),
+                                 (300, 1000), (32768, 128000), (1 << 20, 50000)])
+def test_python_default_block_is_the_librarys(lib, N, V):
+    # The workspace holds one [N, BVc] dL block: the library's default block
+    # and the mirror's must give the same workspace size.
+    p0 = _lib.params(N, 4096, V, bwd_vocab_block=0)
+    bv = tuning.library_default_block(N, V)
+    p1 = _lib.params(N, 4096, V, bwd_vocab_block=bv)
+    assert lib.flce_workspace_size(p0, 1) == lib.flce_workspace_size(p1, 1)
+    if bv > 256:  # a neighbouring block size changes it
+        p2 = _lib.params(N, 4096, V, bwd_vocab_block=bv - 256)
+        assert lib.flce_workspace_size(p2, 1) != lib.flce_workspace_size(p0, 1)
+
+
+@pytest.mark.parametrize("N,V", [(8192, 128256), (16384, 262144), (512, 4096), (1, 7),
+                                 (4096, 32000), (1 << 20, 50000)])
+def test_vocab_block_candidates(N, V):
+    c = tuning.vocab_block_candidates(N, V)
+    vr = tuning.round_up(V, 256)
+    assert c == sorted(set(c), reverse=True)
+    assert tuning.library_default_block(N, V) in c
+    for bv in c:
+        assert bv % 256 == 0 and 256 <= bv <= vr
+        assert N * bv * 2 <= tuning.DEFAULT_DL_BUDGET or bv == tuning.library_default_block(N, V)
+
+
+def test_vocab_block_candidates_llama3_head():
+    # two nearly equal blocks (64256 + 64000) beside the default 65536 + 62720
+    c = tuning.vocab_block_candidates(8192, 128256)
+    assert 65536 in c and 64256 in c and 128256 not in c
+
+
+def test_small_vocab_gets_one_block():
+    assert tuning.vocab_block_candidates(512, 4096)[0] == 4096
+
+
+def test_select_takes_the_fastest_and_keeps_order_on_ties():
+    cfg = tuning.select({"single": 2.0, "pair": 1.5},
+                        {("single", 512): 3.0, ("pair", 512): 3.0, ("pair", 256): 4.0})
+    assert cfg == tuning.FlceConfig("pair", "single", 512)
+    assert cfg.forward_kwargs() == {"gemm_form": "pair"}
+    assert cfg.backward_kwargs() == {"gemm_form": "single", "bwd_vocab_block": 512}
+
+
+def test_gemm_form_parameter():
+    assert _lib.params(4, 64, 10).gemm_form == 0
+    assert _lib.params(4, 64, 10, gemm_form="single").gemm_form == 1
+    assert _lib.params(4, 64, 10, gemm_form="pair").gemm_form == 2
+    assert _lib.params(4, 64, 10, gemm_form=2).gemm_form == 2
+    with pytest.raises(ValueError):
+        _lib.params(4, 64, 10, gemm_form="quad")
+
+
+def test_tune_result_serialises():
+    r = tuning.TuneResult(tuning.FlceConfig("pair", "pair", 65536), {"pair": 1.0},
+                          {("pair", 65536): 2.0}, key=("dev",))
+    d = r.as_dict()
+    assert d["config"]["bwd_vocab_block"] == 65536 and d["backward_ms"] == {"pair/65536": 2.0}
