@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 # step's launches of that kernel) from one ncu capture of this workload's full
 # step (1-pass metrics; profiles/dram_traffic_llama3_head.md). Must be
 # re-measured (or removed) whenever one of these kernels or its raster changes.
-TRAFFIC_PER_LAUNCH = {"fwd_lse": 5.812e9, "bwd_dlogits": 3.341e9, "bwd_dw": 8.644e9,
-                      "bwd_dx": 7.740e9}
+TRAFFIC_PER_LAUNCH = {"fwd_lse": 3.049e9, "bwd_dlogits": 2.916e9, "bwd_dw": 4.040e9,
+                      "bwd_dx": 6.379e9}
 
 
 def peaks():
@@ -273,9 +273,8 @@ def run_ours(args):
         tune = res.as_dict()
     bvb = bkw["bwd_vocab_block"]
     bv_used = bvb or tuning.library_default_block(N, V)
-    env_form = "single" if os.environ.get("FLCE_CTA_PAIR", "1") == "0" else "pair"
-    forms_used = {"forward": fkw.get("gemm_form", "default"), "backward": bkw.get("gemm_form", "default")}
-    forms_used = {k: env_form if f == "default" else f for k, f in forms_used.items()}
+    forms_used = {"forward": F.resolved_gemm_form(N, H, V, fkw.get("gemm_form", "default")),
+                  "backward": F.resolved_gemm_form(N, H, V, bkw.get("gemm_form", "default"))}
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", **opts), dtype=torch.uint8, device=dev)
     bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", bwd_vocab_block=bvb,
                                             **opts), dtype=torch.uint8, device=dev)
@@ -392,7 +391,7 @@ def run_ours(args):
                 "algorithmic_flops_per_step": flops_per[dom],
                 "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
                             and bv_used == tuning.library_default_block(N, V)
-                            and forms_used == {"forward": "pair", "backward": "pair"}
+                            and forms_used == {"forward": "wide", "backward": "wide"}
                             and os.environ.get("FLCE_RASTER", "1") != "0" else None),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
     else:

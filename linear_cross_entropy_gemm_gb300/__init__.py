@@ -27,7 +27,7 @@ __all__ = [
     "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
     "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
     "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace", "flce_saved_size",
-    "GEMM_FORMS",
+    "GEMM_FORMS", "resolved_gemm_form",
 ]
 
 _err_words = {}
@@ -101,6 +101,14 @@ class KernelTrace:
 def flce_workspace_size(N, H, V, which: str, **opts) -> int:
     p = params(N, H, V, **opts)
     return int(_lib.load().flce_workspace_size(p, 0 if which == "forward" else 1))
+
+
+def resolved_gemm_form(N, H, V, gemm_form="default", **opts) -> str:
+    """The GEMM form ("single", "pair" or "wide") calls with these parameters
+    run: ``gemm_form`` itself unless it is "default", else the library default
+    (FLCE_GEMM_FORM in the environment overrides it)."""
+    f = int(_lib.load().flce_resolved_gemm_form(params(N, H, V, gemm_form=gemm_form, **opts)))
+    return {v: k for k, v in GEMM_FORMS.items()}[f]
 
 
 def flce_saved_size(N, H, V, **opts) -> int:

@@ -19,7 +19,7 @@ STATUS_NAMES = {
     6: "FLCE_ERR_TIMEOUT", 7: "FLCE_ERR_UNSUPPORTED",
 }
 # flce_gemm_form_t: "default" leaves the choice to the library.
-GEMM_FORMS = {"default": 0, "single": 1, "pair": 2}
+GEMM_FORMS = {"default": 0, "single": 1, "pair": 2, "wide": 3}
 DEVERR_TARGET = 1
 DEVERR_TIMEOUT = 2
 
@@ -114,6 +114,8 @@ def load() -> ctypes.CDLL:
     lib.flce_selftest_wait_timeout.restype = ctypes.c_int
     lib.flce_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.flce_read_device_error.restype = ctypes.c_int
+    lib.flce_resolved_gemm_form.argtypes = [P]
+    lib.flce_resolved_gemm_form.restype = ctypes.c_int32
     lib.flce_status_string.argtypes = [ctypes.c_int]
     lib.flce_status_string.restype = ctypes.c_char_p
     lib.flce_version.argtypes = []

@@ -73,18 +73,22 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
 
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
-// GEMM kernel form: CTA pairs (cta_group::2, 256 x 256 tiles) or single CTAs
-// (128 x 256 tiles). An explicit gemm_form in the parameters decides; with the
-// default form, FLCE_CTA_PAIR=0 / 1 in the environment overrides the library
-// default (pairs). Both forms compute identical results up to accumulation
-// order.
-bool use_cta_pair(const flce_params_t* p) {
-  if (p->gemm_form == FLCE_GEMM_SINGLE_CTA) return false;
-  if (p->gemm_form == FLCE_GEMM_CTA_PAIR) return true;
-  const char* e = std::getenv("FLCE_CTA_PAIR");
-  if (e && e[0] == '0') return false;
-  if (e && e[0] == '1') return true;
-  return true;
+// GEMM kernel form of a call: an explicit gemm_form decides; with the
+// default form, FLCE_GEMM_FORM=single|pair|wide in the environment overrides
+// the library default (for A/B measurements). All forms compute identical
+// results up to the order of fp32 accumulation inside a tile.
+GemmKind gemm_kind(const flce_params_t* p) {
+  switch (p->gemm_form) {
+    case FLCE_GEMM_SINGLE_CTA: return kGemmSingle;
+    case FLCE_GEMM_CTA_PAIR: return kGemmPair;
+    case FLCE_GEMM_WIDE_PAIR: return kGemmWide;
+    default: break;
+  }
+  const char* e = std::getenv("FLCE_GEMM_FORM");
+  if (e && std::strcmp(e, "single") == 0) return kGemmSingle;
+  if (e && std::strcmp(e, "pair") == 0) return kGemmPair;
+  if (e && std::strcmp(e, "wide") == 0) return kGemmWide;
+  return kGemmWide;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -117,7 +121,7 @@ flce_status_t check_params(const flce_params_t* p) {
   if (p->bwd_vocab_block < 0 || p->bwd_vocab_block % 256 != 0) return FLCE_ERR_INVALID_ARG;
   if (p->has_bias != 0 && p->has_bias != 1) return FLCE_ERR_INVALID_ARG;
   if (p->input_fp16 != 0 && p->input_fp16 != 1) return FLCE_ERR_INVALID_ARG;
-  if (p->gemm_form < FLCE_GEMM_DEFAULT || p->gemm_form > FLCE_GEMM_CTA_PAIR)
+  if (p->gemm_form < FLCE_GEMM_DEFAULT || p->gemm_form > FLCE_GEMM_WIDE_PAIR)
     return FLCE_ERR_INVALID_ARG;
   if (p->vocab_total == 0) {
     if (p->vocab_start != 0) return FLCE_ERR_INVALID_ARG;
@@ -298,6 +302,15 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
 
 extern "C" {
 
+int32_t flce_resolved_gemm_form(const flce_params_t* p) {
+  if (!p) return -1;
+  switch (gemm_kind(p)) {
+    case kGemmSingle: return FLCE_GEMM_SINGLE_CTA;
+    case kGemmWide: return FLCE_GEMM_WIDE_PAIR;
+    default: return FLCE_GEMM_CTA_PAIR;
+  }
+}
+
 size_t flce_workspace_size(const flce_params_t* p, int which) {
   if (check_params(p) != FLCE_OK || p->N == 0) return 0;
   if (which == 0) {
@@ -387,7 +400,8 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   }
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
-  const bool pair = use_cta_pair(p);
+  const GemmKind kind = gemm_kind(p);
+  const bool pair = kind != kGemmSingle;
   CUtensorMap mx, mw;
   if (!encode_2d(&mx, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM, p->input_fp16 != 0) ||
       !encode_2d(&mw, W, H, V, static_cast<uint64_t>(H) * 2, kBK, pair ? kBN / 2 : kBN,
@@ -417,10 +431,10 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
     sa.base = ea;
     sa.probs = sv.probs;
     sa.ld_p = sv.ld_p;
-    le = launch_fwd_store(pair, mx, mw, g, sa, p->has_bias != 0, p->label_smoothing > 0.f,
+    le = launch_fwd_store(kind, mx, mw, g, sa, p->has_bias != 0, p->label_smoothing > 0.f,
                           reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
   } else {
-    le = launch_fwd_lse(pair, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
+    le = launch_fwd_lse(kind, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
                         reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
   }
   if (le != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_LSE)) return FLCE_ERR_CUDA;
@@ -548,7 +562,8 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
   const int64_t bv = vocab_block(p);
   const int nblk = cdiv(V, bv);
   int* derr = reinterpret_cast<int*>(dev_err);
-  const bool pair = use_cta_pair(p);
+  const GemmKind kind = gemm_kind(p);
+  const bool pair = kind != kGemmSingle;
 
   Tracer tr{trace, s};
   if (!tr.begin()) return FLCE_ERR_CUDA;
@@ -630,7 +645,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     da.db_part = w.db_part;
     da.ld_db = static_cast<int>(bv);
     if (!saved) {
-      if (launch_dlogits(pair, mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms),
+      if (launch_dlogits(kind, mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms),
                          s) != cudaSuccess ||
           !tr.after(FLCE_KERNEL_BWD_DLOGITS))
         return FLCE_ERR_CUDA;
@@ -645,7 +660,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     // dW block: one GEMM over all tokens (M = vocab rows, K = tokens).
     GemmGeom g2 = geom(Vb, H, N, f16);
     g2.raster_m_inner = 0;
-    if (use_bands()) g2.band_n = 8;
+    if (use_bands()) g2.band_n = kind == kGemmWide ? 4 : 8;  // 2048 columns of x
     DwArgs wa;
     wa.out = dW;
     wa.out_bf16 = p->dW_fp32 ? 0 : 1;
@@ -655,7 +670,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     wa.row0 = v0;
     wa.Mrows = Vb;
     wa.Ncols = H;
-    if (launch_dw(pair, mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
+    if (launch_dw(kind, mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DW))
       return FLCE_ERR_CUDA;
 
@@ -674,7 +689,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     xa.Ncols = H;
     xa.first = blk == 0;
     xa.last = blk == nblk - 1;
-    if (launch_dx(pair, mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess ||
+    if (launch_dx(kind, mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DX))
       return FLCE_ERR_CUDA;
   }

@@ -21,14 +21,15 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Gemm
   return cudaGetLastError();
 }
 
-// Co-resident 2-CTA clusters of gemm_persistent_pair on the current device,
-// queried once per device (all instantiations share the same footprint).
-static int max_pair_clusters(const void* kernel) {
+// Co-resident 2-CTA clusters of a cluster kernel on the current device,
+// queried once per device and footprint (slot 0: the 256 x 256 pair kernel,
+// whose instantiations share one footprint; slot 1: the wide pair kernel).
+static int max_pair_clusters(const void* kernel, int slot, int threads, size_t smem) {
   constexpr int kMaxDev = 64;
-  static std::atomic<int> cache[kMaxDev];
+  static std::atomic<int> cache[2][kMaxDev];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-  int v = cache[dev].load(std::memory_order_relaxed);
+  int v = cache[slot][dev].load(std::memory_order_relaxed);
   if (v > 0) return v;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -37,15 +38,15 @@ static int max_pair_clusters(const void* kernel) {
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kPairSmemBytes;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   if (cudaOccupancyMaxActiveClusters(&v, kernel, &cfg) != cudaSuccess || v <= 0) {
     cudaGetLastError();
     return 0;
   }
-  cache[dev].store(v, std::memory_order_relaxed);
+  cache[slot][dev].store(v, std::memory_order_relaxed);
   return v;
 }
 
@@ -57,7 +58,8 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kPairSmemBytes));
   if (e != cudaSuccess) return e;
-  int clusters = max_pair_clusters(reinterpret_cast<const void*>(kernel));
+  int clusters = max_pair_clusters(reinterpret_cast<const void*>(kernel), 0, kThreads,
+                                   kPairSmemBytes);
   if (clusters <= 0) clusters = sms / 2;
   const int pair_tiles = ((g.tiles_m + 1) / 2) * g.tiles_n;
   if (clusters > pair_tiles) clusters = pair_tiles;
@@ -66,48 +68,73 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
 }
 
 template <class Epi>
-static cudaError_t launch_any(bool pair, const CUtensorMap& a, const CUtensorMap& b,
-                              const GemmGeom& g, const typename Epi::Args& ea, int* dev_err,
-                              int grid, cudaStream_t st) {
-  return pair ? launch_pair<Epi>(a, b, g, ea, dev_err, grid, st)
-              : launch<Epi>(a, b, g, ea, dev_err, grid, st);
+static cudaError_t launch_wide(const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+                               const typename Epi::Args& ea, int* dev_err, int sms,
+                               cudaStream_t st) {
+  auto kernel = gemm_persistent_wide<Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kWideSmemBytes));
+  if (e != cudaSuccess) return e;
+  int clusters = max_pair_clusters(reinterpret_cast<const void*>(kernel), 1, kWideThreads,
+                                   kWideSmemBytes);
+  if (clusters <= 0) clusters = sms / 2;
+  const int wide_tiles = ((g.tiles_m + 1) / 2) * ((g.tiles_n + 1) / 2);
+  if (clusters > wide_tiles) clusters = wide_tiles;
+  kernel<<<2 * clusters, kWideThreads, kWideSmemBytes, st>>>(a, b, g, ea, dev_err);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_lse(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+template <class Epi>
+static cudaError_t launch_any(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                              const GemmGeom& g, const typename Epi::Args& ea, int* dev_err,
+                              int grid, cudaStream_t st) {
+  switch (kind) {
+    case kGemmWide: return launch_wide<Epi>(a, b, g, ea, dev_err, grid, st);
+    case kGemmPair: return launch_pair<Epi>(a, b, g, ea, dev_err, grid, st);
+    default: return launch<Epi>(a, b, g, ea, dev_err, grid, st);
+  }
+}
+
+cudaError_t launch_fwd_lse(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
                            bool has_smooth, int* dev_err, int grid, cudaStream_t st) {
   if (has_bias)
-    return has_smooth ? launch_any<FwdLseEpi<true, true>>(pair, a, b, g, ea, dev_err, grid, st)
-                      : launch_any<FwdLseEpi<true, false>>(pair, a, b, g, ea, dev_err, grid, st);
-  return has_smooth ? launch_any<FwdLseEpi<false, true>>(pair, a, b, g, ea, dev_err, grid, st)
-                    : launch_any<FwdLseEpi<false, false>>(pair, a, b, g, ea, dev_err, grid, st);
+    return has_smooth ? launch_any<FwdLseEpi<true, true>>(kind, a, b, g, ea, dev_err, grid, st)
+                      : launch_any<FwdLseEpi<true, false>>(kind, a, b, g, ea, dev_err, grid, st);
+  return has_smooth ? launch_any<FwdLseEpi<false, true>>(kind, a, b, g, ea, dev_err, grid, st)
+                    : launch_any<FwdLseEpi<false, false>>(kind, a, b, g, ea, dev_err, grid, st);
 }
 
-cudaError_t launch_fwd_store(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_fwd_store(GemmKind form, const CUtensorMap& a, const CUtensorMap& b,
                              const GemmGeom& g, const FwdStoreArgs& ea, bool has_bias,
                              bool has_smooth, int* dev_err, int grid, cudaStream_t st) {
+  // The storing epilogue (two passes over the accumulator, 512 B of fp16 per
+  // row per 256 columns) is too long to leave exposed between wide tiles.
+  const GemmKind kind = form == kGemmWide ? kGemmPair : form;
   if (has_bias)
-    return has_smooth ? launch_any<FwdStoreEpi<true, true>>(pair, a, b, g, ea, dev_err, grid, st)
-                      : launch_any<FwdStoreEpi<true, false>>(pair, a, b, g, ea, dev_err, grid, st);
-  return has_smooth ? launch_any<FwdStoreEpi<false, true>>(pair, a, b, g, ea, dev_err, grid, st)
-                    : launch_any<FwdStoreEpi<false, false>>(pair, a, b, g, ea, dev_err, grid, st);
+    return has_smooth ? launch_any<FwdStoreEpi<true, true>>(kind, a, b, g, ea, dev_err, grid, st)
+                      : launch_any<FwdStoreEpi<true, false>>(kind, a, b, g, ea, dev_err, grid, st);
+  return has_smooth ? launch_any<FwdStoreEpi<false, true>>(kind, a, b, g, ea, dev_err, grid, st)
+                    : launch_any<FwdStoreEpi<false, false>>(kind, a, b, g, ea, dev_err, grid, st);
 }
 
-cudaError_t launch_dlogits(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_dlogits(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const DlogitsArgs& ea, bool has_bias, int* dev_err,
                            int grid, cudaStream_t st) {
-  return has_bias ? launch_any<DlogitsEpi<true>>(pair, a, b, g, ea, dev_err, grid, st)
-                  : launch_any<DlogitsEpi<false>>(pair, a, b, g, ea, dev_err, grid, st);
+  return has_bias ? launch_any<DlogitsEpi<true>>(kind, a, b, g, ea, dev_err, grid, st)
+                  : launch_any<DlogitsEpi<false>>(kind, a, b, g, ea, dev_err, grid, st);
 }
 
-cudaError_t launch_dw(bool pair, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+cudaError_t launch_dw(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                       const DwArgs& ea, int* dev_err, int grid, cudaStream_t st) {
-  return launch_any<DwEpi>(pair, a, b, g, ea, dev_err, grid, st);
+  return launch_any<DwEpi>(kind, a, b, g, ea, dev_err, grid, st);
 }
 
-cudaError_t launch_dx(bool pair, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+// dx has few output tiles (N/256 x H/256) and a long K: 256 x 512 tiles would
+// leave most of the GPU idle in the last wave, so the wide form runs it as pairs.
+cudaError_t launch_dx(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                       const DxArgs& ea, int* dev_err, int grid, cudaStream_t st) {
-  return launch_any<DxEpi>(pair, a, b, g, ea, dev_err, grid, st);
+  return launch_any<DxEpi>(kind == kGemmWide ? kGemmPair : kind, a, b, g, ea, dev_err, grid, st);
 }
 
 }  // namespace flce

@@ -16,18 +16,21 @@ struct DlogitsArgs;
 struct DwArgs;
 struct DxArgs;
 
-// Persistent tcgen05 GEMMs (flce_gemm.cu). pair = CTA-pair kernel (256 x 256
-// tiles; a K-major B map must then have 128-row boxes). `grid` is the CTA
-// count of the single-CTA kernel (the SM count when it is the smaller).
-cudaError_t launch_fwd_lse(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+// GEMM kernel forms (flce_gemm.cu): one CTA per 128 x 256 tile, a CTA pair per
+// 256 x 256 tile, or a CTA pair per 256 x 512 tile (the dx GEMM runs the wide
+// form as 256 x 256 pairs). The pair forms need 128-row boxes in a K-major B
+// map. `grid` is the CTA count of the single-CTA kernel (the SM count when it
+// is the smaller).
+enum GemmKind : int { kGemmSingle = 0, kGemmPair = 1, kGemmWide = 2 };
+cudaError_t launch_fwd_lse(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
                            bool has_smooth, int* dev_err, int grid, cudaStream_t st);
-cudaError_t launch_dlogits(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_dlogits(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const DlogitsArgs& ea, bool has_bias, int* dev_err,
                            int grid, cudaStream_t st);
-cudaError_t launch_dw(bool pair, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+cudaError_t launch_dw(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                       const DwArgs& ea, int* dev_err, int grid, cudaStream_t st);
-cudaError_t launch_dx(bool pair, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
+cudaError_t launch_dx(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                       const DxArgs& ea, int* dev_err, int grid, cudaStream_t st);
 
 // Row-wise kernels (flce_rowwise.cu).
@@ -87,7 +90,7 @@ cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st);
 int convert_db_parts(int N);
 
 struct FwdStoreArgs;
-cudaError_t launch_fwd_store(bool pair, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_fwd_store(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                              const GemmGeom& g, const FwdStoreArgs& ea, bool has_bias,
                              bool has_smooth, int* dev_err, int grid, cudaStream_t st);
 

@@ -458,4 +458,228 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
+// ---------------------------------------------------------------------------
+// Wide CTA pair: the two CTAs of a cluster compute one 256 x 512 tile as two
+// cta_group::2 MMAs per K step (M=256, N=256 each) that share the A operand.
+// Per stage each CTA loads its 128 rows of A (16 KiB) and two 128-row slices of
+// B, one per N half (2 x 16 KiB): 768 operand rows per 2*256*512 flops against
+// 512 per 2*256*256 for the 256 x 256 pair tile, a quarter fewer bytes moved
+// from L2 into shared memory per flop. The 128 x 512 fp32 accumulator fills
+// all 512 TMEM columns, so there is one accumulator: a tile's epilogue does not
+// overlap the next tile's MMAs (the producer keeps prefetching meanwhile).
+// Eight epilogue warps drain the two 256-column halves at the same time; each
+// half is a 128 x 256 sub-tile for the same epilogues as the other forms.
+//   full[s]  (even CTA) : both CTAs' TMA bytes of stage s
+//   empty[s] (each CTA) : pair MMA commit, multicast to both CTAs
+//   tfull    (each CTA) : pair MMA commit after a tile's last K step
+//   tempty   (even CTA) : 512 epilogue arrivals, 256 from each CTA
+constexpr int kWideStages = 4;
+constexpr int kWideBHalfBytes = (kBN / 2) * kBK * 2;           // 16 KiB
+constexpr int kWideBStageBytes = 2 * kWideBHalfBytes;          // 32 KiB
+constexpr int kWideThreads = 320;
+constexpr int kWideEpiThreads = 256;
+constexpr size_t kWideSmemBytes =
+    1024 + static_cast<size_t>(kWideStages) * (kPairAStageBytes + kWideBStageBytes) +
+    kBarrierBytes;
+
+template <class Epi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
+    gemm_persistent_wide(const __grid_constant__ CUtensorMap mapA,
+                         const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
+                         const typename Epi::Args ea, int* dev_err) {
+  constexpr bool kAMN = Epi::kAMN;
+  constexpr bool kBMN = Epi::kBMN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kWideStages * kPairAStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kWideStages * kWideBStageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kWideStages;
+  uint64_t* tfull = bars + 2 * kWideStages;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* done_bar = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kWideStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, 2 * kWideEpiThreads);
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mapA);
+    tma_prefetch_desc(&mapB);
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Wide tiles: 256 rows of M (two 128-row halves, one per CTA) x 512 columns
+  // of N (two 256-column halves, one per MMA). g's tile counts are in 128-row
+  // and 256-column units; the raster runs over wide tiles.
+  GemmGeom pg = g;
+  pg.tiles_m = (g.tiles_m + 1) / 2;
+  pg.tiles_n = (g.tiles_n + 1) / 2;
+  const int num_tiles = pg.tiles_m * pg.tiles_n;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- TMA producer (both CTAs)
+      const uint64_t pol = l2_policy_evict_normal();
+      const uint32_t full0 = mapa_shared(smem_u32(&full[0]), 0);
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      for (int t = cluster; t < num_tiles; t += nclusters) {
+        int tm2, tn2;
+        tile_coords(pg, t, tm2, tn2);
+        const int m0 = tm2 * (2 * kBM) + static_cast<int>(rank) * kBM;
+        const int n0 = tn2 * (2 * kBN) + static_cast<int>(rank) * (kBN / 2);
+        bool ok = true;
+        for (int kb = 0; kb < g.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, dev_err)) {
+            ok = false;
+            break;
+          }
+          if (leader)
+            mbar_arrive_expect_tx(&full[s], 2 * (kPairAStageBytes + kWideBStageBytes));
+          const uint32_t fb = full0 + static_cast<uint32_t>(s) * 8u;
+          uint8_t* a = sA + s * kPairAStageBytes;
+          uint8_t* b = sB + s * kWideBStageBytes;
+          const int k0 = kb * kBK;
+          if constexpr (!kAMN) {
+            tma_load_2d_pair(a, &mapA, fb, k0 + g.a_k_off, m0 + g.a_mn_off, pol);
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j)
+              tma_load_2d_pair(a + j * kMnBoxBytes, &mapA, fb, m0 + g.a_mn_off + j * 64,
+                               k0 + g.a_k_off, pol);
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint8_t* bh = b + h * kWideBHalfBytes;
+            const int nh = n0 + h * kBN + g.b_mn_off;
+            if constexpr (!kBMN) {
+              tma_load_2d_pair(bh, &mapB, fb, k0 + g.b_k_off, nh, pol);
+            } else {
+#pragma unroll
+              for (int j = 0; j < (kBN / 2) / 64; ++j)
+                tma_load_2d_pair(bh + j * kMnBoxBytes, &mapB, fb, nh + j * 64, k0 + g.b_k_off,
+                                 pol);
+            }
+          }
+          ++issued;
+          if (++s == kWideStages) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: a stage's loads have landed once the pair MMA that read it committed.
+      for (long long i = (issued > kWideStages ? issued - kWideStages : 0); i < issued; ++i)
+        mbar_drain(&empty[i % kWideStages], static_cast<uint32_t>((i / kWideStages) & 1));
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      if (leader) {
+        // ------------------------------------------- MMA issuer (even CTA)
+        const uint32_t idesc = idesc_f16kind_f32(2 * kBM, kBN, kAMN, kBMN, g.ab_fp16 != 0);
+        int s = 0;
+        uint32_t ph = 0;
+        uint32_t aph = 0;
+        for (int t = cluster; t < num_tiles; t += nclusters) {
+          if (!mbar_wait(tempty, aph ^ 1, abort_flag, dev_err)) break;
+          tc_fence_after();
+          bool ok = true;
+          for (int kb = 0; kb < g.k_blocks; ++kb) {
+            if (!mbar_wait(&full[s], ph, abort_flag, dev_err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + s * kPairAStageBytes);
+            const uint32_t b_addr = smem_u32(sB + s * kWideBStageBytes);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUmmaK; ++kk) {
+              const uint64_t ad =
+                  kAMN ? smem_desc_sw128(a_addr + kk * (kUmmaK * 128), kMnBoxBytes, 1024)
+                       : smem_desc_sw128(a_addr + kk * (kUmmaK * 2), 16, 1024);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t bh = b_addr + static_cast<uint32_t>(h * kWideBHalfBytes);
+                const uint64_t bd =
+                    kBMN ? smem_desc_sw128(bh + kk * (kUmmaK * 128), kMnBoxBytes, 1024)
+                         : smem_desc_sw128(bh + kk * (kUmmaK * 2), 16, 1024);
+                umma_bf16_pair(tmem_base + static_cast<uint32_t>(h * kBN), ad, bd, idesc,
+                               (kb | kk) != 0 ? 1u : 0u);
+              }
+            }
+            umma_commit_pair(&empty[s], 0x3);
+            if (++s == kWideStages) {
+              s = 0;
+              ph ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit_pair(tfull, 0x3);
+          aph ^= 1;
+        }
+        umma_commit_pair(done_bar, 0x3);
+      }
+      // Both CTAs: every pair MMA must finish before TMEM is released.
+      mbar_drain(done_bar, 0);
+    }
+  } else {
+    // ------------------------------------------- epilogue (both CTAs, 8 warps)
+    // Warps 2..5 take N half 0, warps 6..9 half 1; warp w reads TMEM lanes
+    // 32 (w % 4) .. 32 (w % 4) + 31.
+    const int half = (warp - 2) >> 2;
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
+    uint32_t aph = 0;
+    for (int t = cluster; t < num_tiles; t += nclusters) {
+      int tm2, tn2;
+      tile_coords(pg, t, tm2, tn2);
+      if (!mbar_wait(tfull, aph, abort_flag, dev_err)) break;
+      tc_fence_after();
+      // The last wide tile's second half can lie wholly past N: no sub-tile.
+      const int tn = tn2 * 2 + half;
+      if (tn < g.tiles_n) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                               static_cast<uint32_t>(half * kBN);
+        Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr);
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(tempty0);
+      aph ^= 1;
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
+}
+
 }  // namespace flce

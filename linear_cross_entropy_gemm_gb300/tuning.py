@@ -1,11 +1,12 @@
 """Per-shape choice of the GEMM form and the backward vocabulary block.
 
-The library defaults (CTA-pair GEMMs; the widest backward vocabulary block
-BVc whose [N, BVc] 16-bit dL staging buffer fits 1 GiB) are tuned for large
-heads. Other shapes can prefer the single-CTA form (fewer, smaller tiles fill
-the 152 SMs better) or another BVc: the block count sets how many dW / dx
-GEMM launches a backward makes, whether dx needs its fp32 accumulator (one
-block does not), and how ragged the last block is.
+The library defaults (wide CTA-pair GEMMs, 256 x 512 tiles; the widest
+backward vocabulary block BVc whose [N, BVc] 16-bit dL staging buffer fits
+1 GiB) are tuned for large heads. Other shapes can prefer the 256 x 256 pair
+or single-CTA forms (more, smaller tiles fill the 152 SMs better) or another
+BVc: the block count sets how many dW / dx GEMM launches a backward makes,
+whether dx needs its fp32 accumulator (one block does not), and how ragged
+the last block is.
 
 ``autotune`` times the candidates through the C ABI on the caller's own
 tensors (CUDA events on the current stream, median of ``reps``) and keeps the
@@ -23,7 +24,7 @@ import torch
 # The library's default staging budget and smallest default block (flce_api.cu).
 DEFAULT_DL_BUDGET = 1 << 30
 MIN_DEFAULT_BLOCK = 4096
-FORMS = ("single", "pair")
+FORMS = ("single", "pair", "wide")
 
 
 @dataclasses.dataclass(frozen=True)

@@ -67,7 +67,7 @@ def test_workspace_sizes(lib):
 @pytest.mark.parametrize("kw,status", [
     (dict(N=-1), 1), (dict(H=0), 1), (dict(V=0), 1), (dict(H=12), 2),
     (dict(label_smoothing=1.5), 1), (dict(lse_square_scale=-1.0), 1),
-    (dict(bwd_vocab_block=100), 1), (dict(gemm_form=3), 1), (dict(gemm_form=-1), 1),
+    (dict(bwd_vocab_block=100), 1), (dict(gemm_form=4), 1), (dict(gemm_form=-1), 1),
 ])
 def test_invalid_params_rejected_on_host(lib, kw, status):
     base = dict(N=4, H=64, V=10)

@@ -14,7 +14,7 @@ from test_gpu_parity import full_check
 
 pytestmark = pytest.mark.gpu
 
-FORMS = ["single", "pair"]
+FORMS = ["single", "pair", "wide"]
 
 CASES = {
     "tiny": (I.WORKLOADS["tiny"], {}),
@@ -45,11 +45,13 @@ def test_forms_compute_the_same_products():
     # the other (they differ only in fp32 accumulation order inside a tile).
     wl = CASES["odd_tiles_ragged"][0]
     a = full_check(wl, gemm_form="single")
-    b = full_check(wl, gemm_form="pair")
-    for k in ("loss", "lse"):
-        assert_loss_close(to_np(a[k]), to_np(b[k]), f"single vs pair {k}")
-    for k in ("dx", "dW", "db"):
-        assert_grad_close(to_np(a[k]), to_np(b[k]).astype(np.float64), f"single vs pair {k}")
+    for other in ("pair", "wide"):
+        b = full_check(wl, gemm_form=other)
+        for k in ("loss", "lse"):
+            assert_loss_close(to_np(a[k]), to_np(b[k]), f"single vs {other} {k}")
+        for k in ("dx", "dW", "db"):
+            assert_grad_close(to_np(a[k]), to_np(b[k]).astype(np.float64),
+                              f"single vs {other} {k}")
 
 
 def test_invalid_gemm_form_is_rejected():
@@ -59,7 +61,7 @@ def test_invalid_gemm_form_is_rejected():
     W = bf16_dev(inp.W, "cuda:0")
     y = torch.from_numpy(inp.y).cuda()
     with pytest.raises(F.FlceError):
-        F.flce_forward(x, W, None, y, gemm_form=3)
+        F.flce_forward(x, W, None, y, gemm_form=4)
 
 
 def _device_inputs(wl):

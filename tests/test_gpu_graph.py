@@ -20,7 +20,7 @@ def _problem(seed):
     return wl, inp
 
 
-@pytest.mark.parametrize("form", ["single", "pair"])
+@pytest.mark.parametrize("form", ["single", "pair", "wide"])
 def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form):
     wl, inp = _problem(41)
     dev = torch.device("cuda:0")

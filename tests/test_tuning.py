@@ -60,9 +60,24 @@ def test_gemm_form_parameter():
     assert _lib.params(4, 64, 10).gemm_form == 0
     assert _lib.params(4, 64, 10, gemm_form="single").gemm_form == 1
     assert _lib.params(4, 64, 10, gemm_form="pair").gemm_form == 2
+    assert _lib.params(4, 64, 10, gemm_form="wide").gemm_form == 3
     assert _lib.params(4, 64, 10, gemm_form=2).gemm_form == 2
     with pytest.raises(ValueError):
         _lib.params(4, 64, 10, gemm_form="quad")
+
+
+def test_resolved_gemm_form(lib, monkeypatch):
+    import linear_cross_entropy_gemm_gb300 as F
+    monkeypatch.delenv("FLCE_GEMM_FORM", raising=False)
+    default = F.resolved_gemm_form(8192, 4096, 128256)
+    assert default in ("pair", "wide")
+    for f in ("single", "pair", "wide"):
+        assert F.resolved_gemm_form(8192, 4096, 128256, gemm_form=f) == f
+        monkeypatch.setenv("FLCE_GEMM_FORM", f)
+        assert F.resolved_gemm_form(8192, 4096, 128256) == f
+        # an explicit form is not overridden by the environment
+        assert F.resolved_gemm_form(8192, 4096, 128256, gemm_form="single") == "single"
+    assert lib.flce_resolved_gemm_form(None) == -1
 
 
 def test_tune_result_serialises():
