@@ -273,8 +273,8 @@ def run_ours(args):
         tune = res.as_dict()
     bvb = bkw["bwd_vocab_block"]
     bv_used = bvb or tuning.library_default_block(N, V)
-    forms_used = {"forward": F.resolved_gemm_form(N, H, V, fkw.get("gemm_form", "default")),
-                  "backward": F.resolved_gemm_form(N, H, V, bkw.get("gemm_form", "default"))}
+    forms_used = {gm: F.resolved_gemm_form(N, H, V, (fkw if gm == "fwd_lse" else bkw).get(
+        "gemm_form", "default"), gemm=gm, bwd_vocab_block=bvb) for gm in F.GEMMS}
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", **opts), dtype=torch.uint8, device=dev)
     bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", bwd_vocab_block=bvb,
                                             **opts), dtype=torch.uint8, device=dev)
@@ -391,7 +391,8 @@ def run_ours(args):
                 "algorithmic_flops_per_step": flops_per[dom],
                 "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
                             and bv_used == tuning.library_default_block(N, V)
-                            and forms_used == {"forward": "wide", "backward": "wide"}
+                            and forms_used == {"fwd_lse": "wide", "bwd_dlogits": "wide",
+                                               "bwd_dw": "wide", "bwd_dx": "pair"}
                             and os.environ.get("FLCE_RASTER", "1") != "0" else None),
                 "traffic_unit": "bytes per launch (ncu dram read + write)"}
     else:

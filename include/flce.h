@@ -70,9 +70,11 @@ typedef enum {
  * the same products; results differ only in the order of fp32 accumulation
  * inside a tile, not in what is summed. */
 typedef enum {
-  FLCE_GEMM_DEFAULT = 0,    /* library default: FLCE_GEMM_WIDE_PAIR (FLCE_GEMM_FORM=
-                               single|pair|wide in the environment overrides the default,
-                               not an explicit form) */
+  FLCE_GEMM_DEFAULT = 0,    /* library default, per GEMM: FLCE_GEMM_WIDE_PAIR where its
+                               K loop has >= 4096 elements and it has >= 608 256 x 512
+                               tiles, else FLCE_GEMM_CTA_PAIR (FLCE_GEMM_FORM=single|pair|
+                               wide in the environment overrides the default, not an
+                               explicit form) */
   FLCE_GEMM_SINGLE_CTA = 1, /* one CTA per 128 x 256 tile (tcgen05 cta_group::1) */
   FLCE_GEMM_CTA_PAIR = 2,   /* two CTAs of a cluster per 256 x 256 tile (cta_group::2) */
   FLCE_GEMM_WIDE_PAIR = 3   /* two CTAs per 256 x 512 tile (two cta_group::2 MMAs per K
@@ -136,10 +138,10 @@ typedef struct {
 size_t flce_workspace_size(const flce_params_t* p, int which);
 
 /* The GEMM form (FLCE_GEMM_SINGLE_CTA, _CTA_PAIR or _WIDE_PAIR) that calls with
- * these parameters use: p->gemm_form if it is not FLCE_GEMM_DEFAULT, else the
- * library default (or the FLCE_GEMM_FORM environment override). Host only;
- * returns -1 for NULL. */
-int32_t flce_resolved_gemm_form(const flce_params_t* p);
+ * these parameters run for one GEMM: which = 0 the forward logits GEMM, 1 the
+ * backward recompute, 2 dW, 3 dx (1 and 2 for the first vocabulary block).
+ * Host only; returns -1 for NULL, invalid parameters or an invalid `which`. */
+int32_t flce_resolved_gemm_form(const flce_params_t* p, int32_t which);
 
 /*
  * Forward. x: [N, H] bf16; W: [V, H] bf16; b: [V] bf16 or NULL (has_bias = 0);

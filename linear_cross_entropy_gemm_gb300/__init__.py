@@ -103,11 +103,18 @@ def flce_workspace_size(N, H, V, which: str, **opts) -> int:
     return int(_lib.load().flce_workspace_size(p, 0 if which == "forward" else 1))
 
 
-def resolved_gemm_form(N, H, V, gemm_form="default", **opts) -> str:
-    """The GEMM form ("single", "pair" or "wide") calls with these parameters
-    run: ``gemm_form`` itself unless it is "default", else the library default
-    (FLCE_GEMM_FORM in the environment overrides it)."""
-    f = int(_lib.load().flce_resolved_gemm_form(params(N, H, V, gemm_form=gemm_form, **opts)))
+GEMMS = ("fwd_lse", "bwd_dlogits", "bwd_dw", "bwd_dx")
+
+
+def resolved_gemm_form(N, H, V, gemm_form="default", gemm="fwd_lse", **opts) -> str:
+    """The GEMM form ("single", "pair" or "wide") that calls with these
+    parameters run for one GEMM (one of ``GEMMS``): ``gemm_form`` itself unless
+    it is "default" (dx runs "wide" as "pair"), else the library's per-GEMM
+    default (FLCE_GEMM_FORM in the environment overrides it)."""
+    f = int(_lib.load().flce_resolved_gemm_form(params(N, H, V, gemm_form=gemm_form, **opts),
+                                               GEMMS.index(gemm)))
+    if f < 0:
+        raise ValueError("flce: invalid parameters")
     return {v: k for k, v in GEMM_FORMS.items()}[f]
 
 

@@ -114,7 +114,7 @@ def load() -> ctypes.CDLL:
     lib.flce_selftest_wait_timeout.restype = ctypes.c_int
     lib.flce_read_device_error.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int32)]
     lib.flce_read_device_error.restype = ctypes.c_int
-    lib.flce_resolved_gemm_form.argtypes = [P]
+    lib.flce_resolved_gemm_form.argtypes = [P, ctypes.c_int32]
     lib.flce_resolved_gemm_form.restype = ctypes.c_int32
     lib.flce_status_string.argtypes = [ctypes.c_int]
     lib.flce_status_string.restype = ctypes.c_char_p

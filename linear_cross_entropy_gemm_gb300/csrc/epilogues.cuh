@@ -1,6 +1,8 @@
-// Epilogues of the FLCE GEMMs. Each runs on the 128 epilogue threads of
-// gemm_persistent; thread i owns row i of the 128 x 256 fp32 accumulator in
-// TMEM and reads it 32 columns at a time.
+// Epilogues of the FLCE GEMMs. Each call drains one 128 x 256 fp32 sub-tile
+// of a CTA's TMEM accumulator with 128 threads (4 warps, one per TMEM lane
+// quarter); thread i owns row i and reads it 32 columns at a time. tm and tn
+// index the sub-tile in 128-row and 256-column units whatever the kernel's
+// tile (a wide 256 x 512 tile is two sub-tiles per CTA on 8 warps).
 //
 // Notation (fla fused_linear_cross_entropy.py; Liger-Kernel PR #239):
 //   z = s * (acc + b_v)          logits of one token row, vocab column v

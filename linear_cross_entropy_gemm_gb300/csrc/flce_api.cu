@@ -13,6 +13,7 @@
 //     dW GEMM       dW[v0:v0+Vb] = dL_blk^T x            (K = all tokens)
 //     dx GEMM       dx (+)= dL_blk W_blk                  (fp32 across blocks)
 //     db finalize   (with a bias)
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -75,8 +76,9 @@ int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // GEMM kernel form of a call: an explicit gemm_form decides; with the
 // default form, FLCE_GEMM_FORM=single|pair|wide in the environment overrides
-// the library default (for A/B measurements). All forms compute identical
-// results up to the order of fp32 accumulation inside a tile.
+// the library default (for A/B measurements), which is chosen per GEMM
+// (gemm_for). All forms compute identical results up to the order of fp32
+// accumulation inside a tile.
 GemmKind gemm_kind(const flce_params_t* p) {
   switch (p->gemm_form) {
     case FLCE_GEMM_SINGLE_CTA: return kGemmSingle;
@@ -88,7 +90,21 @@ GemmKind gemm_kind(const flce_params_t* p) {
   if (e && std::strcmp(e, "single") == 0) return kGemmSingle;
   if (e && std::strcmp(e, "pair") == 0) return kGemmPair;
   if (e && std::strcmp(e, "wide") == 0) return kGemmWide;
-  return kGemmWide;
+  return kGemmAuto;
+}
+
+// The default form of one GEMM D[M, N] = A[M, K] B[N, K]^T. The wide tile's
+// epilogue is not overlapped, so it pays only when the K loop is long enough
+// to amortise it, and its tiles are twice as large, so it needs enough of them
+// to fill the GPU's 76 clusters. Otherwise the 256 x 256 pair is used.
+// Measured on GB300: at K = 4096 (Llama-3 head) the wide step is 2 % faster
+// under the power cap; at K = 2048 the wide forward is 7-16 % slower.
+constexpr int64_t kWideMinK = 4096;
+constexpr int64_t kWideMinTiles = 8 * 76;
+GemmKind gemm_for(GemmKind kind, int64_t M, int64_t N, int64_t K) {
+  if (kind != kGemmAuto) return kind;
+  const int64_t wide_tiles = ((M + 255) / 256) * ((N + 511) / 512);
+  return (K >= kWideMinK && wide_tiles >= kWideMinTiles) ? kGemmWide : kGemmPair;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -302,9 +318,19 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
 
 extern "C" {
 
-int32_t flce_resolved_gemm_form(const flce_params_t* p) {
-  if (!p) return -1;
-  switch (gemm_kind(p)) {
+int32_t flce_resolved_gemm_form(const flce_params_t* p, int32_t which) {
+  if (!p || which < 0 || which > 3 || check_params(p) != FLCE_OK) return -1;
+  const int64_t N = p->N, H = p->H, V = p->V;
+  const int64_t Vb = std::min<int64_t>(vocab_block(p), V);
+  const GemmKind kind = gemm_kind(p);
+  GemmKind k;
+  switch (which) {
+    case 0: k = gemm_for(kind, N, V, H); break;
+    case 1: k = gemm_for(kind, N, Vb, H); break;
+    case 2: k = gemm_for(kind, Vb, H, N); break;
+    default: k = kind == kGemmSingle ? kGemmSingle : kGemmPair; break;  // dx
+  }
+  switch (k) {
     case kGemmSingle: return FLCE_GEMM_SINGLE_CTA;
     case kGemmWide: return FLCE_GEMM_WIDE_PAIR;
     default: return FLCE_GEMM_CTA_PAIR;
@@ -400,7 +426,7 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   }
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
-  const GemmKind kind = gemm_kind(p);
+  const GemmKind kind = gemm_for(gemm_kind(p), p->N, p->V, p->H);
   const bool pair = kind != kGemmSingle;
   CUtensorMap mx, mw;
   if (!encode_2d(&mx, x, H, N, static_cast<uint64_t>(H) * 2, kBK, kBM, p->input_fp16 != 0) ||
@@ -645,7 +671,8 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     da.db_part = w.db_part;
     da.ld_db = static_cast<int>(bv);
     if (!saved) {
-      if (launch_dlogits(kind, mx_k, mw_k, g1, da, p->has_bias != 0, derr, grid_for(g1, sms),
+      if (launch_dlogits(gemm_for(kind, N, Vb, H), mx_k, mw_k, g1, da, p->has_bias != 0, derr,
+                         grid_for(g1, sms),
                          s) != cudaSuccess ||
           !tr.after(FLCE_KERNEL_BWD_DLOGITS))
         return FLCE_ERR_CUDA;
@@ -660,7 +687,8 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     // dW block: one GEMM over all tokens (M = vocab rows, K = tokens).
     GemmGeom g2 = geom(Vb, H, N, f16);
     g2.raster_m_inner = 0;
-    if (use_bands()) g2.band_n = kind == kGemmWide ? 4 : 8;  // 2048 columns of x
+    const GemmKind k2 = gemm_for(kind, Vb, H, N);
+    if (use_bands()) g2.band_n = k2 == kGemmWide ? 4 : 8;  // 2048 columns of x
     DwArgs wa;
     wa.out = dW;
     wa.out_bf16 = p->dW_fp32 ? 0 : 1;
@@ -670,7 +698,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     wa.row0 = v0;
     wa.Mrows = Vb;
     wa.Ncols = H;
-    if (launch_dw(kind, mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
+    if (launch_dw(k2, mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DW))
       return FLCE_ERR_CUDA;
 
@@ -689,7 +717,8 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     xa.Ncols = H;
     xa.first = blk == 0;
     xa.last = blk == nblk - 1;
-    if (launch_dx(kind, mdl_k, mw_mn, g3, xa, derr, grid_for(g3, sms), s) != cudaSuccess ||
+    if (launch_dx(kind == kGemmSingle ? kGemmSingle : kGemmPair, mdl_k, mw_mn, g3, xa, derr,
+                  grid_for(g3, sms), s) != cudaSuccess ||
         !tr.after(FLCE_KERNEL_BWD_DX))
       return FLCE_ERR_CUDA;
   }

@@ -90,8 +90,8 @@ static cudaError_t launch_any(GemmKind kind, const CUtensorMap& a, const CUtenso
                               int grid, cudaStream_t st) {
   switch (kind) {
     case kGemmWide: return launch_wide<Epi>(a, b, g, ea, dev_err, grid, st);
-    case kGemmPair: return launch_pair<Epi>(a, b, g, ea, dev_err, grid, st);
-    default: return launch<Epi>(a, b, g, ea, dev_err, grid, st);
+    case kGemmSingle: return launch<Epi>(a, b, g, ea, dev_err, grid, st);
+    default: return launch_pair<Epi>(a, b, g, ea, dev_err, grid, st);  // kGemmAuto is resolved earlier
   }
 }
 

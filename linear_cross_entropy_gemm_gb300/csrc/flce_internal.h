@@ -21,7 +21,8 @@ struct DxArgs;
 // form as 256 x 256 pairs). The pair forms need 128-row boxes in a K-major B
 // map. `grid` is the CTA count of the single-CTA kernel (the SM count when it
 // is the smaller).
-enum GemmKind : int { kGemmSingle = 0, kGemmPair = 1, kGemmWide = 2 };
+// kGemmAuto is resolved per GEMM on the host before any launch.
+enum GemmKind : int { kGemmSingle = 0, kGemmPair = 1, kGemmWide = 2, kGemmAuto = 3 };
 cudaError_t launch_fwd_lse(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
                            bool has_smooth, int* dev_err, int grid, cudaStream_t st);

@@ -11,6 +11,9 @@
 //               lane) i; drains tile t while the MMAs of tile t+1 run
 // The tile loop is persistent (tile = blockIdx.x + j * gridDim.x), in an
 // order chosen per problem so the operand shared by concurrent CTAs stays in L2.
+// Two cluster forms follow the single-CTA one: gemm_persistent_pair (two CTAs,
+// cta_group::2, one 256 x 256 tile) and gemm_persistent_wide (two CTAs, one
+// 256 x 512 tile as two MMAs per K step sharing A, 8 epilogue warps).
 //
 // Operands are 128-byte-swizzled bf16 tiles loaded by TMA, either K-major
 // (rows of 64 contiguous K elements) or MN-major (rows of 64 contiguous M/N

@@ -66,18 +66,38 @@ def test_gemm_form_parameter():
         _lib.params(4, 64, 10, gemm_form="quad")
 
 
-def test_resolved_gemm_form(lib, monkeypatch):
+@pytest.mark.parametrize("N,H,V,expect", [
+    # Llama-3 head: every GEMM long enough and large enough for 256 x 512 tiles
+    (8192, 4096, 128256, dict(fwd_lse="wide", bwd_dlogits="wide", bwd_dw="wide")),
+    # H = 2048: the logits GEMMs' K loop is too short; dW has too few wide tiles
+    (32768, 2048, 128000, dict(fwd_lse="pair", bwd_dlogits="pair", bwd_dw="pair")),
+    (4096, 2048, 32000, dict(fwd_lse="pair", bwd_dlogits="pair", bwd_dw="pair")),
+    (16384, 4096, 262144, dict(fwd_lse="wide", bwd_dlogits="wide", bwd_dw="wide")),
+    (512, 256, 4096, dict(fwd_lse="pair", bwd_dlogits="pair", bwd_dw="pair")),
+])
+def test_default_form_per_gemm(lib, monkeypatch, N, H, V, expect):
     import linear_cross_entropy_gemm_gb300 as F
     monkeypatch.delenv("FLCE_GEMM_FORM", raising=False)
-    default = F.resolved_gemm_form(8192, 4096, 128256)
-    assert default in ("pair", "wide")
+    for gm, f in expect.items():
+        assert F.resolved_gemm_form(N, H, V, gemm=gm) == f, gm
+    assert F.resolved_gemm_form(N, H, V, gemm="bwd_dx") == "pair"
+
+
+def test_explicit_and_environment_forms(lib, monkeypatch):
+    import linear_cross_entropy_gemm_gb300 as F
+    monkeypatch.delenv("FLCE_GEMM_FORM", raising=False)
     for f in ("single", "pair", "wide"):
-        assert F.resolved_gemm_form(8192, 4096, 128256, gemm_form=f) == f
+        # an explicit form applies to every GEMM at any size (dx runs wide as pair)
+        for gm in F.GEMMS:
+            want = "pair" if (gm == "bwd_dx" and f == "wide") else f
+            assert F.resolved_gemm_form(512, 256, 4096, gemm_form=f, gemm=gm) == want
         monkeypatch.setenv("FLCE_GEMM_FORM", f)
-        assert F.resolved_gemm_form(8192, 4096, 128256) == f
-        # an explicit form is not overridden by the environment
-        assert F.resolved_gemm_form(8192, 4096, 128256, gemm_form="single") == "single"
-    assert lib.flce_resolved_gemm_form(None) == -1
+        assert F.resolved_gemm_form(512, 256, 4096) == f
+        # the environment does not override an explicit form
+        assert F.resolved_gemm_form(512, 256, 4096, gemm_form="single") == "single"
+    assert lib.flce_resolved_gemm_form(None, 0) == -1
+    assert lib.flce_resolved_gemm_form(_lib.params(4, 64, 10), 4) == -1
+    assert lib.flce_resolved_gemm_form(_lib.params(4, 12, 10), 0) == -1  # invalid H
 
 
 def test_tune_result_serialises():
