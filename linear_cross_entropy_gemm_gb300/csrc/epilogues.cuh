@@ -82,6 +82,92 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
   return v[0];
 }
 
+// p ? a : b as one selp. A chain of selects that picks v[j] for j == k would
+// otherwise be turned into the indexed load v[k], which puts v in local memory.
+__device__ __forceinline__ float select_f32(bool p, float a, float b) {
+  float r;
+  asm("{\n\t.reg .pred q;\n\tsetp.ne.s32 q, %3, 0;\n\tselp.f32 %0, %1, %2, q;\n\t}"
+      : "=f"(r)
+      : "f"(a), "f"(b), "r"(static_cast<int>(p)));
+  return r;
+}
+
+// ------------------------------------------------------- coalesced stores
+// A warp holds a 32 x 32 block one row per lane (v[j] = element (lane, j)).
+// Stored straight from registers, every warp store instruction would touch 32
+// rows, 16 bytes each. Instead the block passes through the warp's own
+// kStageBytes staging buffer in shared memory, in 16-byte slots XOR-swizzled by
+// row so that both the row-wise writes and the column-wise reads are free of
+// bank conflicts. It leaves as whole row segments: each store instruction
+// writes 4 rows x 128 bytes (fp32) or 8 rows x 64 bytes (16-bit). Only rows <
+// nrows and columns < ncols are written; gbase is element (0, 0), rows are ld
+// elements apart and 16-byte aligned. The buffer (kStageBytes, from the GEMM
+// engine) belongs to the calling warp alone.
+
+__device__ __forceinline__ void store_block_f32(float* __restrict__ gbase, size_t ld, int nrows,
+                                                int ncols, const float (&v)[32], void* stage_raw,
+                                                int lane) {
+  float4* stage = static_cast<float4*>(stage_raw);
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    stage[lane * 8 + (q ^ (lane & 7))] =
+        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  __syncwarp();
+  const int qq = lane & 7;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const float4 u = stage[r * 8 + (qq ^ (r & 7))];
+    if (r < nrows) {
+      float* o = gbase + static_cast<size_t>(r) * ld + 4 * qq;
+      if (4 * qq + 4 <= ncols) {
+        *reinterpret_cast<float4*>(o) = u;
+      } else {
+        if (4 * qq + 0 < ncols) o[0] = u.x;
+        if (4 * qq + 1 < ncols) o[1] = u.y;
+        if (4 * qq + 2 < ncols) o[2] = u.z;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// As store_block_f32, rounded to the 16-bit operand type (bf16, or fp16).
+__device__ __forceinline__ void store_block_16(uint16_t* __restrict__ gbase, size_t ld, int nrows,
+                                               int ncols, const float (&v)[32], bool fp16,
+                                               void* stage_raw, int lane) {
+  uint4* stage = static_cast<uint4*>(stage_raw);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 u;
+    u.x = pack_16x2(v[8 * q + 0], v[8 * q + 1], fp16);
+    u.y = pack_16x2(v[8 * q + 2], v[8 * q + 3], fp16);
+    u.z = pack_16x2(v[8 * q + 4], v[8 * q + 5], fp16);
+    u.w = pack_16x2(v[8 * q + 6], v[8 * q + 7], fp16);
+    stage[lane * 4 + (q ^ ((lane >> 1) & 3))] = u;
+  }
+  __syncwarp();
+  const int qq = lane & 3;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = 8 * i + (lane >> 2);
+    const uint4 u = stage[r * 4 + (qq ^ ((r >> 1) & 3))];
+    if (r < nrows) {
+      uint16_t* o = gbase + static_cast<size_t>(r) * ld + 8 * qq;
+      if (8 * qq + 8 <= ncols) {
+        *reinterpret_cast<uint4*>(o) = u;
+      } else {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (8 * qq + e < ncols)
+            o[e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
+      }
+    }
+  }
+  __syncwarp();
+}
+
 // ------------------------------------------------------------------ forward
 // Folds each logits tile into per-(row, vocab tile) base-2 online-softmax
 // partials (m = max z log2e, d = sum 2^(z log2e - m)), the tile's sum of z
@@ -105,33 +191,70 @@ struct FwdLseEpi {
   static constexpr bool kAMN = false, kBMN = false;
   using Args = FwdLseArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr) {
+                              int, int, uint32_t taddr, void*) {
     const int row = tm * kBM + row_in_tile;
     const int v0 = tn * kBN;
     const int64_t yv = row < a.Ntok ? __ldg(a.y + row) - a.y_off : -1;
     const int ty = (yv >= v0 && yv < static_cast<int64_t>(v0) + kBN) ? static_cast<int>(yv - v0) : -1;
-    float m = -INFINITY, d = 0.f, S = 0.f, zt = 0.f;
+    // With u = acc + b, z log2e = c2 u: one FFMA per logit feeds the ex2, and
+    // a chunk's maximum of z log2e is c2 times its maximum of u (its minimum
+    // when c2 < 0). S and the target logit are kept in units of u and scaled
+    // once at the end.
+    const float c2 = a.scale * kLog2e;
+    const bool neg = c2 < 0.f;
+    float m = -INFINITY, d = 0.f, S = 0.f, ut = 0.f;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
-      float v[32], bv[32];
+      float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
       const int col0 = v0 + c * 32;
-      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
-      float cm = -INFINITY;
+      const bool full = col0 + 32 <= a.V;  // the same for the whole warp
+      if constexpr (HAS_BIAS) {
+        float bv[32];
+        load_bias32<true>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float z = (v[j] + bv[j]) * a.scale;
-        const bool ok = col0 + j < a.V;
-        if constexpr (HAS_SMOOTH) S += ok ? z : 0.f;
-        zt = (c * 32 + j == ty) ? z : zt;
-        v[j] = ok ? z * kLog2e : -INFINITY;
-        cm = fmaxf(cm, v[j]);
+        for (int j = 0; j < 32; ++j) v[j] += bv[j];
+      }
+      if ((ty >> 5) == c) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) ut = select_f32(j == (ty & 31), v[j], ut);
+      }
+      float cm;
+      if (full) {
+        if constexpr (HAS_SMOOTH) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) S += v[j];
+        }
+        float e = v[0];
+        if (neg) {
+#pragma unroll
+          for (int j = 1; j < 32; ++j) e = fminf(e, v[j]);
+        } else {
+#pragma unroll
+          for (int j = 1; j < 32; ++j) e = fmaxf(e, v[j]);
+        }
+        cm = e * c2;
+      } else {
+        // The last vocabulary tile: columns >= V do not exist.
+        cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const bool ok = col0 + j < a.V;
+          if constexpr (HAS_SMOOTH) S += ok ? v[j] : 0.f;
+          cm = ok ? fmaxf(cm, v[j] * c2) : cm;
+        }
       }
       const float nm = fmaxf(m, cm);
       if (nm != -INFINITY) {
         float acc = d * fast_exp2(m - nm);
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc += fast_exp2(v[j] - nm);
+          for (int j = 0; j < 32; ++j) acc += fast_exp2(fmaf(v[j], c2, -nm));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            acc += (col0 + j < a.V) ? fast_exp2(fmaf(v[j], c2, -nm)) : 0.f;
+        }
         d = acc;
         m = nm;
       }
@@ -140,8 +263,8 @@ struct FwdLseEpi {
       const size_t o = static_cast<size_t>(tn) * a.Ntok + row;
       a.part_m[o] = m;
       a.part_d[o] = d;
-      if constexpr (HAS_SMOOTH) a.part_s[o] = S;
-      if (ty >= 0) a.zy[row] = zt;
+      if constexpr (HAS_SMOOTH) a.part_s[o] = S * a.scale;
+      if (ty >= 0) a.zy[row] = ut * a.scale;
     }
   }
 };
@@ -163,7 +286,7 @@ struct FwdStoreEpi {
   static constexpr bool kAMN = false, kBMN = false;
   using Args = FwdStoreArgs;
   __device__ static void tile(const Args& A, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr) {
+                              int, int, uint32_t taddr, void*) {
     const FwdLseArgs& a = A.base;
     const int row = tm * kBM + row_in_tile;
     const int v0 = tn * kBN;
@@ -254,8 +377,9 @@ struct DlogitsEpi {
   static constexpr bool kAMN = false, kBMN = false;
   using Args = DlogitsArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int lane, int quad, uint32_t taddr) {
+                              int lane, int quad, uint32_t taddr, void* stage) {
     const int row = tm * kBM + row_in_tile;
+    const int row0 = tm * kBM + quad * 32;  // the warp's first row (lane = row - row0)
     const bool row_ok = row < a.Ntok;
     const int vt0 = tn * kBN;  // block-relative
     const int vg0 = a.v0 + vt0;
@@ -263,26 +387,44 @@ struct DlogitsEpi {
     const float dls = __ldg(a.dl_scale);
     const int64_t yv = row_ok ? __ldg(a.y + row) - a.y_off : -1;
     const int ty = (yv >= vg0 && yv < static_cast<int64_t>(vg0) + kBN) ? static_cast<int>(yv - vg0) : -1;
+    // p = 2^(c2 (acc + b) - lse2) with c2 = s log2e: one FFMA per logit feeds
+    // the ex2, one more gives a p - c; the target column subtracts t.
+    const float c2 = a.scale * kLog2e;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
-      float v[32], bv[32];
+      float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
       const int colb0 = vt0 + c * 32;
       const int colg0 = vg0 + c * 32;
-      load_bias32<HAS_BIAS>(a.bias, colg0 < a.V ? colg0 : 0, a.V, bv, a.fp16 != 0);
+      if constexpr (HAS_BIAS) {
+        float bv[32];
+        load_bias32<true>(a.bias, colg0 < a.V ? colg0 : 0, a.V, bv, a.fp16 != 0);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float z = (v[j] + bv[j]) * a.scale;
-        const float p = fast_exp2(fmaf(z, kLog2e, -cf.x));
-        float dl = fmaf(cf.y, p, -cf.z);
-        dl -= (c * 32 + j == ty) ? cf.w : 0.f;
-        v[j] = (row_ok && colb0 + j < a.Vb) ? dl : 0.f;
+        for (int j = 0; j < 32; ++j) v[j] += bv[j];
       }
-      if (row_ok) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = fmaf(cf.y, fast_exp2(fmaf(v[j], c2, -cf.x)), -cf.z);
+      if ((ty >> 5) == c) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] -= (j == (ty & 31)) ? cf.w : 0.f;
+      }
+      // Rows past N (their 2^(...) is not bounded) and columns past the block are 0.
+      if (!row_ok) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.f;
+      }
+      if (colb0 + 32 > a.Vb) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = (colb0 + j < a.Vb) ? v[j] : 0.f;
+      }
+      uint16_t* dst = a.dL + static_cast<size_t>(row0) * a.ld_dL + colb0;
+      if (dls == 1.f) {
+        store_block_16(dst, a.ld_dL, a.Ntok - row0, 32, v, a.fp16 != 0, stage, lane);
+      } else {
         float sv[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) sv[j] = v[j] * dls;
-        store32_16(a.dL + static_cast<size_t>(row) * a.ld_dL + colb0, sv, a.fp16 != 0);
+        store_block_16(dst, a.ld_dL, a.Ntok - row0, 32, sv, a.fp16 != 0, stage, lane);
       }
       if constexpr (HAS_BIAS) {
         const float colsum = warp_column_sums(v, lane);
@@ -311,11 +453,11 @@ struct DwArgs {
 struct DwEpi {
   static constexpr bool kAMN = true, kBMN = true;
   using Args = DwArgs;
-  __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr) {
-    const int r = tm * kBM + row_in_tile;
-    const bool row_ok = r < a.Mrows;
-    const size_t orow = static_cast<size_t>(a.row0 + (row_ok ? r : 0)) * a.ld;
+  __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int,
+                              int lane, int quad, uint32_t taddr, void* stage) {
+    const int r0 = tm * kBM + quad * 32;  // the warp's first block-relative row
+    const int nrows = a.Mrows - r0;
+    const size_t obase = static_cast<size_t>(a.row0 + (nrows > 0 ? r0 : 0)) * a.ld;
     const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
@@ -324,34 +466,14 @@ struct DwEpi {
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] *= sc;
       const int col0 = tn * kBN + c * 32;
-      if (row_ok && col0 < a.Ncols) store_dw(a, orow, col0, v);
-    }
-  }
-  __device__ __forceinline__ static void store_dw(const Args& a, size_t orow, int col0,
-                                                 const float (&v)[32]) {
-    {
-      if (a.out_bf16) {
-        uint16_t* o = reinterpret_cast<uint16_t*>(a.out) + orow + col0;
-        if (col0 + 32 <= a.Ncols) {
-          store32_16(o, v, a.fp16 != 0);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < a.Ncols - col0) o[j] = to16(v[j], a.fp16 != 0);
-        }
-      } else {
-        float* o = reinterpret_cast<float*>(a.out) + orow + col0;
-        if (col0 + 32 <= a.Ncols) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(o)[q] =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < a.Ncols - col0) o[j] = v[j];
-        }
-      }
+      if (col0 >= a.Ncols) continue;  // uniform over the warp
+      const int ncols = min(32, a.Ncols - col0);
+      if (a.out_bf16)
+        store_block_16(reinterpret_cast<uint16_t*>(a.out) + obase + col0, a.ld, nrows, ncols, v,
+                       a.fp16 != 0, stage, lane);
+      else
+        store_block_f32(reinterpret_cast<float*>(a.out) + obase + col0, a.ld, nrows, ncols, v,
+                        stage, lane);
     }
   }
 };
@@ -376,7 +498,7 @@ struct DxEpi {
   static constexpr bool kAMN = false, kBMN = true;
   using Args = DxArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr) {
+                              int, int, uint32_t taddr, void*) {
     const int row = tm * kBM + row_in_tile;
     const bool row_ok = row < a.Ntok;
     const size_t orow = static_cast<size_t>(row_ok ? row : 0) * a.ld;

@@ -39,8 +39,12 @@ constexpr int kEpiThreads = 128;
 constexpr int kTmemCols = 2 * kBN;
 constexpr int kMnBoxBytes = 64 * kBK * 2;     // one 64 (MN) x 64 (K) MN-major box
 constexpr int kBarrierBytes = 256;
-constexpr size_t kSmemBytes =
-    1024 + static_cast<size_t>(kStages) * (kAStageBytes + kBStageBytes) + kBarrierBytes;
+// Per epilogue warp: a staging buffer through which the epilogues transpose
+// 32 x 32 blocks for coalesced global stores.
+constexpr int kStageBytes = 4096;
+constexpr size_t kSmemBytes = 1024 +
+                              static_cast<size_t>(kStages) * (kAStageBytes + kBStageBytes) +
+                              4 * kStageBytes + kBarrierBytes;
 
 struct GemmGeom {
   int M, N, K;
@@ -100,7 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kAStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kStages * kBStageBytes);
+  uint8_t* stage = sB + kStages * kBStageBytes;  // 4 epilogue warps x kStageBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + 4 * kStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kStages;
   uint64_t* tfull = bars + 2 * kStages;
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      Epi::tile(ea, g, tm, tn, row_in_tile, lane, quad, taddr);
+      Epi::tile(ea, g, tm, tn, row_in_tile, lane, quad, taddr, stage + (warp - 2) * kStageBytes);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -272,7 +277,7 @@ constexpr int kPairAStageBytes = kBM * kBK * 2;         // 16 KiB
 constexpr int kPairBStageBytes = (kBN / 2) * kBK * 2;   // 16 KiB
 constexpr size_t kPairSmemBytes =
     1024 + static_cast<size_t>(kPairStages) * (kPairAStageBytes + kPairBStageBytes) +
-    kBarrierBytes;
+    4 * kStageBytes + kBarrierBytes;
 
 template <class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -286,7 +291,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kPairStages * kPairAStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kPairStages * kPairBStageBytes);
+  uint8_t* stage = sB + kPairStages * kPairBStageBytes;  // 4 epilogue warps x kStageBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + 4 * kStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kPairStages;
   uint64_t* tfull = bars + 2 * kPairStages;
@@ -446,7 +452,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr);
+      Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr,
+                stage + (warp - 2) * kStageBytes);
       tc_fence_before();
       mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
       acc ^= 1;
@@ -483,7 +490,7 @@ constexpr int kWideThreads = 320;
 constexpr int kWideEpiThreads = 256;
 constexpr size_t kWideSmemBytes =
     1024 + static_cast<size_t>(kWideStages) * (kPairAStageBytes + kWideBStageBytes) +
-    kBarrierBytes;
+    8 * kStageBytes + kBarrierBytes;
 
 template <class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
@@ -497,7 +504,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kWideStages * kPairAStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + kWideStages * kWideBStageBytes);
+  uint8_t* stage = sB + kWideStages * kWideBStageBytes;  // 8 epilogue warps x kStageBytes
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + 8 * kStageBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kWideStages;
   uint64_t* tfull = bars + 2 * kWideStages;
@@ -670,7 +678,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
       if (tn < g.tiles_n) {
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(half * kBN);
-        Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr);
+        Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr,
+                  stage + (warp - 2) * kStageBytes);
       }
       tc_fence_before();
       mbar_arrive_cluster(tempty0);
@@ -684,5 +693,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
+
+static_assert(kSmemBytes <= 232448 && kPairSmemBytes <= 232448 && kWideSmemBytes <= 232448,
+              "dynamic shared memory above the 227 KiB a CTA may use");
 
 }  // namespace flce
