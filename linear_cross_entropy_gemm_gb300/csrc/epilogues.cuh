@@ -82,6 +82,40 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Reductions of 32 values as pairwise trees (depth 5 instead of a 31-long
+// dependent chain: with two epilogue warps per SM sub-partition the chain's
+// latency is not hidden).
+__device__ __forceinline__ float tree_max32(const float (&v)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fmaxf(v[i], v[i + 16]);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+  return t[0];
+}
+__device__ __forceinline__ float tree_min32(const float (&v)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = fminf(v[i], v[i + 16]);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] = fminf(t[i], t[i + w]);
+  return t[0];
+}
+__device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
+  float t[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) t[i] = v[i] + v[i + 16];
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] += t[i + w];
+  return t[0];
+}
+
 // p ? a : b as one selp. A chain of selects that picks v[j] for j == k would
 // otherwise be turned into the indexed load v[k], which puts v in local memory.
 __device__ __forceinline__ float select_f32(bool p, float a, float b) {
@@ -221,19 +255,8 @@ struct FwdLseEpi {
       }
       float cm;
       if (full) {
-        if constexpr (HAS_SMOOTH) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) S += v[j];
-        }
-        float e = v[0];
-        if (neg) {
-#pragma unroll
-          for (int j = 1; j < 32; ++j) e = fminf(e, v[j]);
-        } else {
-#pragma unroll
-          for (int j = 1; j < 32; ++j) e = fmaxf(e, v[j]);
-        }
-        cm = e * c2;
+        if constexpr (HAS_SMOOTH) S += tree_sum32(v);
+        cm = (neg ? tree_min32(v) : tree_max32(v)) * c2;
       } else {
         // The last vocabulary tile: columns >= V do not exist.
         cm = -INFINITY;
@@ -249,7 +272,8 @@ struct FwdLseEpi {
         float acc = d * fast_exp2(m - nm);
         if (full) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc += fast_exp2(fmaf(v[j], c2, -nm));
+          for (int j = 0; j < 32; ++j) v[j] = fast_exp2(fmaf(v[j], c2, -nm));
+          acc += tree_sum32(v);
         } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j)
@@ -461,12 +485,14 @@ struct DwEpi {
     const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
+      const int col0 = tn * kBN + c * 32;
+      if (col0 >= a.Ncols) break;  // uniform over the warp
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
+      if (sc != 1.f) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] *= sc;
-      const int col0 = tn * kBN + c * 32;
-      if (col0 >= a.Ncols) continue;  // uniform over the warp
+        for (int j = 0; j < 32; ++j) v[j] *= sc;
+      }
       const int ncols = min(32, a.Ncols - col0);
       if (a.out_bf16)
         store_block_16(reinterpret_cast<uint16_t*>(a.out) + obase + col0, a.ld, nrows, ncols, v,
