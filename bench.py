@@ -250,14 +250,17 @@ def run_ours(args):
     if args.shape:
         n_, h_, v_ = (int(t) for t in args.shape.split(","))
         wl = wl.with_(name=f"{wl.name}-shape", N=n_, H=h_, V=v_)
+    if args.dtype != wl.dtype:
+        wl = wl.with_(dtype=args.dtype)
+    tdt = torch.float16 if args.dtype == "fp16" else torch.bfloat16
     pk = peaks()
 
     inp = I.make_inputs(wl)
-    host_x = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host_x = torch.from_numpy(inp.x.view(np.int16)).view(tdt).pin_memory()
     host_y = torch.from_numpy(inp.y).pin_memory()
     host_dl = torch.from_numpy(inp.dloss).pin_memory()
     x = host_x.to(dev)
-    W = torch.from_numpy(inp.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(inp.W.view(np.int16)).view(tdt).to(dev)
     y = host_y.to(dev)
     dloss = host_dl.to(dev)
     opts = dict(ignore_index=wl.ignore_index, label_smoothing=wl.label_smoothing,
@@ -280,7 +283,7 @@ def run_ours(args):
                                             **opts), dtype=torch.uint8, device=dev)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
-    dx = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty(N, H, dtype=tdt, device=dev)
     dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -329,7 +332,8 @@ def run_ours(args):
     # ---- stored-probability backward (no logits recompute), same timing rules
     stored = None
     if not args.no_stored_mode:
-        saved = torch.empty(F.flce_saved_size(N, H, V, **opts), dtype=torch.uint8, device=dev)
+        saved = torch.empty(F.flce_saved_size(N, H, V, input_fp16=args.dtype == "fp16", **opts),
+                            dtype=torch.uint8, device=dev)
 
         def step_stored(trace=False):
             F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), saved=saved,
@@ -390,6 +394,7 @@ def run_ours(args):
                 "ms_per_step": dom_ms_per_step,
                 "algorithmic_flops_per_step": flops_per[dom],
                 "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
+                            and args.dtype == "bf16"
                             and bv_used == tuning.library_default_block(N, V)
                             and forms_used == {"fwd_lse": "wide", "bwd_dlogits": "wide",
                                                "bwd_dw": "wide", "bwd_dx": "pair"}
@@ -406,9 +411,10 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": value / (ws * N / (PAGES_MS * 1e-3)),
-        "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{wl.name}: N={N} H={H} V={V} bf16, mean, no bias, dloss=1",
+        "vs_baseline": (value / (ws * N / (PAGES_MS * 1e-3)) if args.dtype == "bf16" and
+                        (N, H, V) == (8192, 4096, 128256) else None),
+        "dtype": args.dtype, "data": "synthetic",
+        "config": {"workload": f"{wl.name}: N={N} H={H} V={V} {args.dtype}, mean, no bias, dloss=1",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "l2": "flushed (256 MiB write) before each timed step, outside the events",
                    "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
@@ -448,6 +454,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="N,H,V override (profiling captures only)")
     ap.add_argument("--no-stored-mode", action="store_true")
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
+                    help="operand type (the headline workload is bf16; fp16 is a side measurement)")
     ap.add_argument("--autotune", action="store_true",
                     help="time the GEMM forms and backward vocabulary blocks first and run the "
                          "fastest (tuning.autotune); the table goes into the JSON line")
