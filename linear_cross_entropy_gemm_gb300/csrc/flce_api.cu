@@ -181,7 +181,7 @@ struct FwdWs {
 size_t carve_fwd(const flce_params_t* p, void* base, FwdWs* w) {
   const size_t N = static_cast<size_t>(p->N);
   const size_t NT = static_cast<size_t>(cdiv(p->V, kBN));
-  const size_t nblk = static_cast<size_t>(cdiv(p->N, kMergeThreads));
+  const size_t nblk = static_cast<size_t>(cdiv(p->N, kMergeRows));
   Carver c(base, 0);
   w->part_m = c.take<float>(NT * N);
   w->part_d = c.take<float>(NT * N);
@@ -762,7 +762,7 @@ flce_status_t flce_loss_from_stats(const flce_params_t* p, const float* stats, c
     return FLCE_OK;
   }
   if (!stats || !y || !lse || !workspace) return FLCE_ERR_INVALID_ARG;
-  const int nblk = cdiv(N, kMergeThreads);
+  const int nblk = cdiv(N, kMergeRows);
   Carver c(workspace, 0);
   double* blk_sum = c.take<double>(nblk);
   int* blk_cnt = c.take<int>(nblk);

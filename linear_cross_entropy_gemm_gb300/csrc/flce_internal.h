@@ -51,7 +51,8 @@ struct MergeArgs {
   int* blk_cnt;         // [blocks]
   int* dev_err;
 };
-constexpr int kMergeThreads = 256;
+constexpr int kMergeRows = 32;   // token rows per merge block (one per lane)
+constexpr int kMergeSplit = 8;   // warps per merge block, each folding every 8th vocab tile
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st);
 cudaError_t launch_finalize(const MergeArgs& a, cudaStream_t st);
 

@@ -45,26 +45,69 @@ __device__ __forceinline__ void block_sum(double& v, int& c) {
   __syncthreads();
 }
 
-// lse from base-2 partials: M = max m_t, D = sum d_t 2^(m_t - M),
-// lse = (M + log2 D) ln 2 (the (m, d) merge of online softmax).
-template <bool HAS_SMOOTH>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  double l = 0.0;
-  int valid = 0;
-  if (row < a.N) {
-    float M = -INFINITY, D = 0.f, S = 0.f;
-    const float* pm = a.part_m + row;
-    const float* pd = a.part_d + row;
-    for (int t = 0; t < a.NT; ++t) {
-      const size_t o = static_cast<size_t>(t) * a.N;
-      const float m = __ldg(pm + o);
-      const float d = __ldg(pd + o);
+// Folds one token row's per-vocab-tile base-2 partials (m_t, d_t, S_t) into
+// M = max m_t, D = sum d_t 2^(m_t - M), S = sum S_t, in the one fixed order
+// both the loss merge and the vocabulary-shard statistics use (so a single
+// shard reproduces the plain call bit for bit). A block takes kMergeRows rows
+// (lane = row: each load of one vocab tile's partials is one coalesced
+// 128-byte segment); warp w folds tiles w, w + kMergeSplit, ...; warp 0 then
+// merges the kMergeSplit results in warp order. Returns true in warp 0, whose
+// M, D, S hold the row's result; the other warps may leave.
+__device__ __forceinline__ bool fold_partials(const float* part_m, const float* part_d,
+                                              const float* part_s, int N, int NT, float& M,
+                                              float& D, float& S) {
+  __shared__ float sm[kMergeSplit][kMergeRows], sd[kMergeSplit][kMergeRows],
+      ss[kMergeSplit][kMergeRows];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int row = blockIdx.x * kMergeRows + lane;
+  M = -INFINITY;
+  D = 0.f;
+  S = 0.f;
+  if (row < N) {
+#pragma unroll 4
+    for (int t = w; t < NT; t += kMergeSplit) {
+      const size_t o = static_cast<size_t>(t) * N + row;
+      const float m = __ldg(part_m + o);
+      const float d = __ldg(part_d + o);
       const float nm = fmaxf(M, m);
       D = D * fast_exp2(M - nm) + d * fast_exp2(m - nm);
       M = nm;
-      if constexpr (HAS_SMOOTH) S += __ldg(a.part_s + row + o);
+      if (part_s) S += __ldg(part_s + o);
     }
+  }
+  sm[w][lane] = M;
+  sd[w][lane] = D;
+  ss[w][lane] = S;
+  __syncthreads();
+  if (w != 0) return false;
+  M = sm[0][lane];
+  D = sd[0][lane];
+  S = ss[0][lane];
+#pragma unroll
+  for (int k = 1; k < kMergeSplit; ++k) {
+    const float m = sm[k][lane];
+    const float nm = fmaxf(M, m);
+    if (nm != -INFINITY) {  // a warp with no vocab tile keeps (-inf, 0)
+      D = D * fast_exp2(M - nm) + sd[k][lane] * fast_exp2(m - nm);
+      M = nm;
+    }
+    S += ss[k][lane];
+  }
+  return true;
+}
+
+// lse = (M + log2 D) ln 2 (the (m, d) merge of online softmax), then the
+// per-token loss and, for sum / mean, the block's loss sum (fixed order).
+template <bool HAS_SMOOTH>
+__global__ void __launch_bounds__(kMergeRows * kMergeSplit) merge_kernel(const MergeArgs a) {
+  float M, D, S;
+  if (!fold_partials(a.part_m, a.part_d, HAS_SMOOTH ? a.part_s : nullptr, a.N, a.NT, M, D, S))
+    return;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * kMergeRows + lane;
+  double l = 0.0;
+  int valid = 0;
+  if (row < a.N) {
     const double lse = (static_cast<double>(M) + log2(static_cast<double>(D))) * kLn2;
     a.lse[row] = static_cast<float>(lse);
     const int64_t yv = a.y[row];
@@ -82,8 +125,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     if (a.reduction == 0) a.loss[row] = static_cast<float>(l);
   }
   if (a.reduction != 0) {
-    block_sum(l, valid);
-    if (threadIdx.x == 0) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      l += __shfl_down_sync(0xffffffffu, l, o);
+      valid += __shfl_down_sync(0xffffffffu, valid, o);
+    }
+    if (lane == 0) {
       a.blk_sum[blockIdx.x] = l;
       a.blk_cnt[blockIdx.x] = valid;
     }
@@ -106,16 +153,16 @@ __global__ void finalize_loss_kernel(const double* blk_sum, const int* blk_cnt, 
 }
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t st) {
-  const int blocks = (a.N + kMergeThreads - 1) / kMergeThreads;
+  const int blocks = (a.N + kMergeRows - 1) / kMergeRows;
   if (a.part_s)
-    merge_kernel<true><<<blocks, kMergeThreads, 0, st>>>(a);
+    merge_kernel<true><<<blocks, kMergeRows * kMergeSplit, 0, st>>>(a);
   else
-    merge_kernel<false><<<blocks, kMergeThreads, 0, st>>>(a);
+    merge_kernel<false><<<blocks, kMergeRows * kMergeSplit, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_finalize(const MergeArgs& a, cudaStream_t st) {
-  const int blocks = (a.N + kMergeThreads - 1) / kMergeThreads;
+  const int blocks = (a.N + kMergeRows - 1) / kMergeRows;
   finalize_loss_kernel<<<1, 1024, 0, st>>>(a.blk_sum, a.blk_cnt, blocks, a.reduction, a.loss);
   return cudaGetLastError();
 }
@@ -302,19 +349,12 @@ int convert_db_parts(int N) { return (N + kConvRows - 1) / kConvRows; }
 // One shard's per-token statistics over its vocabulary rows: the (m, d)
 // merge of its tile partials, its sum of z, and z_y when the target falls in
 // the shard (0 otherwise, so a SUM across shards yields z_y exactly once).
-__global__ void __launch_bounds__(256) shard_stats_kernel(const ShardStatsArgs a) {
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(kMergeRows * kMergeSplit)
+    shard_stats_kernel(const ShardStatsArgs a) {
+  float M, D, S;
+  if (!fold_partials(a.part_m, a.part_d, a.part_s, a.N, a.NT, M, D, S)) return;
+  const int row = blockIdx.x * kMergeRows + (threadIdx.x & 31);
   if (row >= a.N) return;
-  float M = -INFINITY, D = 0.f, S = 0.f;
-  for (int t = 0; t < a.NT; ++t) {
-    const size_t o = static_cast<size_t>(t) * a.N + row;
-    const float m = a.part_m[o];
-    const float d = a.part_d[o];
-    const float nm = fmaxf(M, m);
-    D = D * fast_exp2(M - nm) + d * fast_exp2(m - nm);
-    M = nm;
-    if (a.part_s) S += a.part_s[o];
-  }
   const int64_t yv = a.y[row];
   float zy = 0.f;
   if (yv != a.ignore_index) {
@@ -331,7 +371,7 @@ __global__ void __launch_bounds__(256) shard_stats_kernel(const ShardStatsArgs a
 }
 
 cudaError_t launch_shard_stats(const ShardStatsArgs& a, cudaStream_t st) {
-  shard_stats_kernel<<<(a.N + 255) / 256, 256, 0, st>>>(a);
+  shard_stats_kernel<<<(a.N + kMergeRows - 1) / kMergeRows, kMergeRows * kMergeSplit, 0, st>>>(a);
   return cudaGetLastError();
 }
 
