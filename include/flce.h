@@ -140,7 +140,9 @@ size_t flce_workspace_size(const flce_params_t* p, int which);
 /* The GEMM form (FLCE_GEMM_SINGLE_CTA, _CTA_PAIR or _WIDE_PAIR) that calls with
  * these parameters run for one GEMM: which = 0 the forward logits GEMM, 1 the
  * backward recompute, 2 dW, 3 dx (1 and 2 for the first vocabulary block).
- * Host only; returns -1 for NULL, invalid parameters or an invalid `which`. */
+ * The dx GEMM and the forward of flce_forward_store run a wide form as
+ * CTA pairs. Host only; returns -1 for NULL, invalid parameters or an invalid
+ * `which`. */
 int32_t flce_resolved_gemm_form(const flce_params_t* p, int32_t which);
 
 /*
