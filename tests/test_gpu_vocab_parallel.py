@@ -25,8 +25,14 @@ def _sim_allreduce(tensors):
     return run
 
 
+@pytest.mark.parametrize("form", ["default", "single", "wide"])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-def test_uneven_shards_match_whole_vocabulary(reduction):
+def test_uneven_shards_match_whole_vocabulary(reduction, form, monkeypatch):
+    # The shard calls take no gemm_form of their own: the environment override
+    # selects the kernel form for every call of the test (shard offsets in the
+    # wide and single-CTA kernels as well as the default pairs).
+    if form != "default":
+        monkeypatch.setenv("FLCE_GEMM_FORM", form)
     wl = I.Workload("vp", N=300, H=264, V=3001, seed=41, b_std=0.3, ignore_frac=0.1,
                     label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.8,
                     reduction=reduction,
