@@ -24,7 +24,9 @@ import torch
 # The library's default staging budget and smallest default block (flce_api.cu).
 DEFAULT_DL_BUDGET = 1 << 30
 MIN_DEFAULT_BLOCK = 4096
-FORMS = ("single", "pair", "wide")
+# "default" is the library's own per-GEMM choice, so the tuner never does
+# worse than a plain call (up to timing noise).
+FORMS = ("default", "single", "pair", "wide")
 
 
 @dataclasses.dataclass(frozen=True)
