@@ -126,51 +126,42 @@ __device__ __forceinline__ float select_f32(bool p, float a, float b) {
   return r;
 }
 
-// ------------------------------------------------------- coalesced stores
+// ------------------------------------------------- asynchronous block stores
 // A warp holds a 32 x 32 block one row per lane (v[j] = element (lane, j)).
-// Stored straight from registers, every warp store instruction would touch 32
-// rows, 16 bytes each. Instead the block passes through the warp's own
-// kStageBytes staging buffer in shared memory, in 16-byte slots XOR-swizzled by
-// row so that both the row-wise writes and the column-wise reads are free of
-// bank conflicts. It leaves as whole row segments: each store instruction
-// writes 4 rows x 128 bytes (fp32) or 8 rows x 64 bytes (16-bit). Only rows <
-// nrows and columns < ncols are written; gbase is element (0, 0), rows are ld
-// elements apart and 16-byte aligned. The buffer (kStageBytes, from the GEMM
-// engine) belongs to the calling warp alone.
-
-__device__ __forceinline__ void store_block_f32(float* __restrict__ gbase, size_t ld, int nrows,
-                                                int ncols, const float (&v)[32], void* stage_raw,
-                                                int lane) {
+// It writes the block into its own staging buffer in shared memory in the
+// layout of a TMA box with the tensor map's swizzle (16-byte slots XOR-ed by
+// row, which also keeps the writes free of bank conflicts), and one lane hands
+// the box to the TMA engine. The global write then completes in the
+// background, overlapping whatever the SM does next (in the 256 x 512 kernel,
+// the next tile's MMAs); the tensor map clips rows and columns outside the
+// output. The buffer is rewritten only once the previous store has read it;
+// the kernel waits for all stores before it exits. (x, y) = (column, row) of
+// the block's first element.
+//   fp32   : 32 rows x 128 B, map swizzle 128B: slot q of row r at r*8 + (q ^ (r & 7))
+//   16-bit : 32 rows x 64 B,  map swizzle 64B:  slot q of row r at r*4 + (q ^ ((r >> 1) & 3))
+__device__ __forceinline__ void tma_block_f32(const CUtensorMap* map, int x, int y,
+                                              const float (&v)[32], void* stage_raw, int lane) {
   float4* stage = static_cast<float4*>(stage_raw);
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
 #pragma unroll
   for (int q = 0; q < 8; ++q)
     stage[lane * 8 + (q ^ (lane & 7))] =
         make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  fence_proxy_async_smem();
   __syncwarp();
-  const int qq = lane & 7;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int r = 4 * i + (lane >> 3);
-    const float4 u = stage[r * 8 + (qq ^ (r & 7))];
-    if (r < nrows) {
-      float* o = gbase + static_cast<size_t>(r) * ld + 4 * qq;
-      if (4 * qq + 4 <= ncols) {
-        *reinterpret_cast<float4*>(o) = u;
-      } else {
-        if (4 * qq + 0 < ncols) o[0] = u.x;
-        if (4 * qq + 1 < ncols) o[1] = u.y;
-        if (4 * qq + 2 < ncols) o[2] = u.z;
-      }
-    }
+  if (lane == 0) {
+    tma_store_2d(map, stage, x, y);
+    bulk_commit_group();
   }
-  __syncwarp();
 }
 
-// As store_block_f32, rounded to the 16-bit operand type (bf16, or fp16).
-__device__ __forceinline__ void store_block_16(uint16_t* __restrict__ gbase, size_t ld, int nrows,
-                                               int ncols, const float (&v)[32], bool fp16,
-                                               void* stage_raw, int lane) {
+__device__ __forceinline__ void tma_block_16(const CUtensorMap* map, int x, int y,
+                                             const float (&v)[32], bool fp16, void* stage_raw,
+                                             int lane) {
   uint4* stage = static_cast<uint4*>(stage_raw);
+  if (lane == 0) bulk_wait_group_read0();
+  __syncwarp();
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 u;
@@ -180,26 +171,12 @@ __device__ __forceinline__ void store_block_16(uint16_t* __restrict__ gbase, siz
     u.w = pack_16x2(v[8 * q + 6], v[8 * q + 7], fp16);
     stage[lane * 4 + (q ^ ((lane >> 1) & 3))] = u;
   }
+  fence_proxy_async_smem();
   __syncwarp();
-  const int qq = lane & 3;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = 8 * i + (lane >> 2);
-    const uint4 u = stage[r * 4 + (qq ^ ((r >> 1) & 3))];
-    if (r < nrows) {
-      uint16_t* o = gbase + static_cast<size_t>(r) * ld + 8 * qq;
-      if (8 * qq + 8 <= ncols) {
-        *reinterpret_cast<uint4*>(o) = u;
-      } else {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (8 * qq + e < ncols)
-            o[e] = static_cast<uint16_t>((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu));
-      }
-    }
+  if (lane == 0) {
+    tma_store_2d(map, stage, x, y);
+    bulk_commit_group();
   }
-  __syncwarp();
 }
 
 // ------------------------------------------------------------------ forward
@@ -390,10 +367,9 @@ struct DlogitsArgs {
   int Ntok;
   int v0;              // first vocab id of the block
   int Vb;              // vocab ids in the block
-  uint16_t* dL;        // [Ntok, ld_dL], block-relative columns
-  int ld_dL;
   float* db_part;      // [tiles_m * 4, ld_db] or null
   int ld_db;
+  CUtensorMap dl_map;  // TMA store map of the dL block: [Ntok rows, Vb columns], 16-bit
 };
 
 template <bool HAS_BIAS>
@@ -441,14 +417,15 @@ struct DlogitsEpi {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = (colb0 + j < a.Vb) ? v[j] : 0.f;
       }
-      uint16_t* dst = a.dL + static_cast<size_t>(row0) * a.ld_dL + colb0;
-      if (dls == 1.f) {
-        store_block_16(dst, a.ld_dL, a.Ntok - row0, 32, v, a.fp16 != 0, stage, lane);
-      } else {
-        float sv[32];
+      if (row0 < a.Ntok && colb0 < a.Vb) {  // the same for the whole warp
+        if (dls == 1.f) {
+          tma_block_16(&a.dl_map, colb0, row0, v, a.fp16 != 0, stage, lane);
+        } else {
+          float sv[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = v[j] * dls;
-        store_block_16(dst, a.ld_dL, a.Ntok - row0, 32, sv, a.fp16 != 0, stage, lane);
+          for (int j = 0; j < 32; ++j) sv[j] = v[j] * dls;
+          tma_block_16(&a.dl_map, colb0, row0, sv, a.fp16 != 0, stage, lane);
+        }
       }
       if constexpr (HAS_BIAS) {
         const float colsum = warp_column_sums(v, lane);
@@ -464,12 +441,10 @@ struct DlogitsEpi {
 // ---------------------------------------------------------- backward: dW
 // dW[v0 + r, :] = sum_n dL[n, r] x[n, :] for block-relative vocab row r.
 struct DwArgs {
-  void* out;      // dW [V, ld] fp32, or the 16-bit operand type
-  int out_bf16;   // 1: write the 16-bit type (bf16, or fp16 when fp16)
+  CUtensorMap out_map;  // TMA store map of this block's dW rows: [Mrows, Ncols], fp32 or 16-bit
+  int out_bf16;   // 1: dW is the 16-bit type (bf16, or fp16 when fp16)
   int fp16;
   const float* acc_scale;  // [0]: undoes the dL scale (power of two)
-  int ld;         // H
-  int row0;       // v0
   int Mrows;      // Vb
   int Ncols;      // H
 };
@@ -480,8 +455,6 @@ struct DwEpi {
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int,
                               int lane, int quad, uint32_t taddr, void* stage) {
     const int r0 = tm * kBM + quad * 32;  // the warp's first block-relative row
-    const int nrows = a.Mrows - r0;
-    const size_t obase = static_cast<size_t>(a.row0 + (nrows > 0 ? r0 : 0)) * a.ld;
     const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
@@ -493,13 +466,11 @@ struct DwEpi {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] *= sc;
       }
-      const int ncols = min(32, a.Ncols - col0);
+      if (r0 >= a.Mrows) continue;  // the same for the whole warp
       if (a.out_bf16)
-        store_block_16(reinterpret_cast<uint16_t*>(a.out) + obase + col0, a.ld, nrows, ncols, v,
-                       a.fp16 != 0, stage, lane);
+        tma_block_16(&a.out_map, col0, r0, v, a.fp16 != 0, stage, lane);
       else
-        store_block_f32(reinterpret_cast<float*>(a.out) + obase + col0, a.ld, nrows, ncols, v,
-                        stage, lane);
+        tma_block_f32(&a.out_map, col0, r0, v, stage, lane);
     }
   }
 };

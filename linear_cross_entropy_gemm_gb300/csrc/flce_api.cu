@@ -72,6 +72,24 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// TMA store map of a row-major [outer, inner] output for the epilogues'
+// 32 x 32 blocks: fp32 with the 128-byte swizzle (128-byte box rows) or a
+// 16-bit type with the 64-byte swizzle (64-byte box rows), the staging layouts
+// of epilogues.cuh. Stores are clipped to [inner, outer].
+bool encode_store_2d(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer,
+                     uint64_t pitch_bytes, bool fp32) {
+  auto fn = encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, base,
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            fp32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int cdiv(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 // GEMM kernel form of a call: an explicit gemm_form decides; with the
@@ -666,10 +684,10 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     da.Ntok = N;
     da.v0 = v0;
     da.Vb = Vb;
-    da.dL = w.dL;
-    da.ld_dL = static_cast<int>(bv);
     da.db_part = w.db_part;
     da.ld_db = static_cast<int>(bv);
+    if (!encode_store_2d(&da.dl_map, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, false))
+      return FLCE_ERR_CUDA;
     if (!saved) {
       if (launch_dlogits(gemm_for(kind, N, Vb, H), mx_k, mw_k, g1, da, p->has_bias != 0, derr,
                          grid_for(g1, sms),
@@ -690,12 +708,14 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     const GemmKind k2 = gemm_for(kind, Vb, H, N);
     if (use_bands()) g2.band_n = k2 == kGemmWide ? 4 : 8;  // 2048 columns of x
     DwArgs wa;
-    wa.out = dW;
+    const size_t dw_elt = p->dW_fp32 ? 4 : 2;
+    if (!encode_store_2d(&wa.out_map,
+                         static_cast<char*>(dW) + static_cast<size_t>(v0) * H * dw_elt, H, Vb,
+                         static_cast<uint64_t>(H) * dw_elt, p->dW_fp32 != 0))
+      return FLCE_ERR_CUDA;
     wa.out_bf16 = p->dW_fp32 ? 0 : 1;
     wa.fp16 = p->input_fp16;
     wa.acc_scale = w.dl_scale + 1;
-    wa.ld = H;
-    wa.row0 = v0;
     wa.Mrows = Vb;
     wa.Ncols = H;
     if (launch_dw(k2, mdl_mn, mx_mn, g2, wa, derr, grid_for(g2, sms), s) != cudaSuccess ||

@@ -96,7 +96,7 @@ template <class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_persistent(const __grid_constant__ CUtensorMap mapA,
                     const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
-                    const typename Epi::Args ea, int* dev_err) {
+                    const __grid_constant__ typename Epi::Args ea, int* dev_err) {
   constexpr bool kAMN = Epi::kAMN;
   constexpr bool kBMN = Epi::kBMN;
   extern __shared__ uint8_t smem_raw[];
@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's epilogue stores have completed
   }
   __syncwarp();
   tc_fence_before();
@@ -283,7 +284,7 @@ template <class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_persistent_pair(const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
-                         const typename Epi::Args ea, int* dev_err) {
+                         const __grid_constant__ typename Epi::Args ea, int* dev_err) {
   constexpr bool kAMN = Epi::kAMN;
   constexpr bool kBMN = Epi::kBMN;
   extern __shared__ uint8_t smem_raw[];
@@ -459,6 +460,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's epilogue stores have completed
   }
   __syncwarp();
   tc_fence_before();
@@ -496,7 +498,7 @@ template <class Epi>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
     gemm_persistent_wide(const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
-                         const typename Epi::Args ea, int* dev_err) {
+                         const __grid_constant__ typename Epi::Args ea, int* dev_err) {
   constexpr bool kAMN = Epi::kAMN;
   constexpr bool kBMN = Epi::kBMN;
   extern __shared__ uint8_t smem_raw[];
@@ -685,6 +687,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
       mbar_arrive_cluster(tempty0);
       aph ^= 1;
     }
+    if (lane == 0) bulk_wait_group0();  // this warp's epilogue stores have completed
   }
   __syncwarp();
   tc_fence_before();
