@@ -1,8 +1,13 @@
 // Epilogues of the FLCE GEMMs. Each call drains one 128 x 256 fp32 sub-tile
-// of a CTA's TMEM accumulator with 128 threads (4 warps, one per TMEM lane
-// quarter); thread i owns row i and reads it 32 columns at a time. tm and tn
-// index the sub-tile in 128-row and 256-column units whatever the kernel's
-// tile (a wide 256 x 512 tile is two sub-tiles per CTA on 8 warps).
+// of a CTA's TMEM accumulator, or the chunks of it that an EpiSlice names,
+// with 128 threads (4 warps, one per TMEM lane quarter); thread i owns row i
+// and reads it 32 columns at a time. tm and tn index the sub-tile in 128-row
+// and 256-column units whatever the kernel's tile (a wide 256 x 512 tile is
+// two sub-tiles per CTA on 8 warps, or on 16 with each sub-tile's columns
+// split between two warps).
+//
+// Each epilogue states kWideWarps, the epilogue warps it runs with in the
+// 256 x 512 kernel, and kStageNeed, the shared staging bytes a warp uses.
 //
 // Notation (fla fused_linear_cross_entropy.py; Liger-Kernel PR #239):
 //   z = s * (acc + b_v)          logits of one token row, vocab column v
@@ -200,9 +205,10 @@ struct FwdLseArgs {
 template <bool HAS_BIAS, bool HAS_SMOOTH>
 struct FwdLseEpi {
   static constexpr bool kAMN = false, kBMN = false;
+  static constexpr int kWideWarps = 16, kStageNeed = 0;
   using Args = FwdLseArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr, void*) {
+                              int lane, int, uint32_t taddr, void*, const EpiSlice& sl) {
     const int row = tm * kBM + row_in_tile;
     const int v0 = tn * kBN;
     const int64_t yv = row < a.Ntok ? __ldg(a.y + row) - a.y_off : -1;
@@ -215,7 +221,7 @@ struct FwdLseEpi {
     const bool neg = c2 < 0.f;
     float m = -INFINITY, d = 0.f, S = 0.f, ut = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = sl.c_lo; c < sl.c_hi; ++c) {
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
       const int col0 = v0 + c * 32;
@@ -260,12 +266,29 @@ struct FwdLseEpi {
         m = nm;
       }
     }
+    // The target column lies in at most one warp's chunks.
+    const bool has_t = ty >= 0 && (ty >> 5) >= sl.c_lo && (ty >> 5) < sl.c_hi;
+    if (row < a.Ntok && has_t) a.zy[row] = ut * a.scale;
+    if (sl.sub == 1) {
+      // Second half of a column-split sub-tile: hand (m, d, S) to the partner.
+      sl.xchg[lane] = make_float4(m, d, S, 0.f);
+      mbar_arrive(sl.xbar);
+      return;
+    }
+    if (sl.sub == 0) {
+      if (!mbar_wait(sl.xbar, sl.xph, sl.abort_flag, sl.dev_err)) return;
+      const float4 o = sl.xchg[lane];
+      const float nm = fmaxf(m, o.x);
+      // A half whose columns all lie past V has m = -inf and d = 0.
+      d = nm == -INFINITY ? 0.f : d * fast_exp2(m - nm) + o.y * fast_exp2(o.x - nm);
+      m = nm;
+      S += o.z;
+    }
     if (row < a.Ntok) {
       const size_t o = static_cast<size_t>(tn) * a.Ntok + row;
       a.part_m[o] = m;
       a.part_d[o] = d;
       if constexpr (HAS_SMOOTH) a.part_s[o] = S * a.scale;
-      if (ty >= 0) a.zy[row] = ut * a.scale;
     }
   }
 };
@@ -285,9 +308,11 @@ struct FwdStoreArgs {
 template <bool HAS_BIAS, bool HAS_SMOOTH>
 struct FwdStoreEpi {
   static constexpr bool kAMN = false, kBMN = false;
+  // Two passes over the whole sub-tile: never column-split (it runs on pairs).
+  static constexpr int kWideWarps = 8, kStageNeed = 0;
   using Args = FwdStoreArgs;
   __device__ static void tile(const Args& A, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr, void*) {
+                              int, int, uint32_t taddr, void*, const EpiSlice&) {
     const FwdLseArgs& a = A.base;
     const int row = tm * kBM + row_in_tile;
     const int v0 = tn * kBN;
@@ -375,9 +400,13 @@ struct DlogitsArgs {
 template <bool HAS_BIAS>
 struct DlogitsEpi {
   static constexpr bool kAMN = false, kBMN = false;
+  // With a bias the db column sums need the registers of 8 warps (16 spill).
+  static constexpr int kWideWarps = HAS_BIAS ? 8 : 16;
+  static constexpr int kStageNeed = 32 * 32 * 2;  // one 16-bit 32 x 32 box
   using Args = DlogitsArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int lane, int quad, uint32_t taddr, void* stage) {
+                              int lane, int quad, uint32_t taddr, void* stage,
+                              const EpiSlice& sl) {
     const int row = tm * kBM + row_in_tile;
     const int row0 = tm * kBM + quad * 32;  // the warp's first row (lane = row - row0)
     const bool row_ok = row < a.Ntok;
@@ -391,7 +420,7 @@ struct DlogitsEpi {
     // the ex2, one more gives a p - c; the target column subtracts t.
     const float c2 = a.scale * kLog2e;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = sl.c_lo; c < sl.c_hi; ++c) {
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
       const int colb0 = vt0 + c * 32;
@@ -451,13 +480,15 @@ struct DwArgs {
 
 struct DwEpi {
   static constexpr bool kAMN = true, kBMN = true;
+  static constexpr int kWideWarps = 8, kStageNeed = 32 * 32 * 4;  // one fp32 32 x 32 box
   using Args = DwArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int,
-                              int lane, int quad, uint32_t taddr, void* stage) {
+                              int lane, int quad, uint32_t taddr, void* stage,
+                              const EpiSlice& sl) {
     const int r0 = tm * kBM + quad * 32;  // the warp's first block-relative row
     const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = sl.c_lo; c < sl.c_hi; ++c) {
       const int col0 = tn * kBN + c * 32;
       if (col0 >= a.Ncols) break;  // uniform over the warp
       float v[32];
@@ -493,15 +524,16 @@ struct DxArgs {
 
 struct DxEpi {
   static constexpr bool kAMN = false, kBMN = true;
+  static constexpr int kWideWarps = 8, kStageNeed = 0;
   using Args = DxArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr, void*) {
+                              int, int, uint32_t taddr, void*, const EpiSlice& sl) {
     const int row = tm * kBM + row_in_tile;
     const bool row_ok = row < a.Ntok;
     const size_t orow = static_cast<size_t>(row_ok ? row : 0) * a.ld;
     const float sc = __ldg(a.acc_scale);
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = sl.c_lo; c < sl.c_hi; ++c) {
       float v[32];
       tmem_ld_32cols(taddr + c * 32, v);
 #pragma unroll

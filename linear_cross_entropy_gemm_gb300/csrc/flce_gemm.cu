@@ -1,5 +1,6 @@
 // Instantiations and launchers of the persistent tcgen05 GEMMs.
 #include <atomic>
+#include <cstdlib>
 
 #include <cuda_runtime.h>
 
@@ -23,10 +24,11 @@ static cudaError_t launch(const CUtensorMap& a, const CUtensorMap& b, const Gemm
 
 // Co-resident 2-CTA clusters of a cluster kernel on the current device,
 // queried once per device and footprint (slot 0: the 256 x 256 pair kernel,
-// whose instantiations share one footprint; slot 1: the wide pair kernel).
+// whose instantiations share one footprint; slots 1 and 2: the wide pair
+// kernel with 8 and 16 epilogue warps).
 static int max_pair_clusters(const void* kernel, int slot, int threads, size_t smem) {
   constexpr int kMaxDev = 64;
-  static std::atomic<int> cache[2][kMaxDev];
+  static std::atomic<int> cache[3][kMaxDev];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   int v = cache[slot][dev].load(std::memory_order_relaxed);
@@ -67,21 +69,40 @@ static cudaError_t launch_pair(const CUtensorMap& a, const CUtensorMap& b, const
   return cudaGetLastError();
 }
 
+template <class Epi, int kEW>
+static cudaError_t launch_wide_warps(const CUtensorMap& a, const CUtensorMap& b,
+                                     const GemmGeom& g, const typename Epi::Args& ea,
+                                     int* dev_err, int sms, cudaStream_t st) {
+  auto kernel = gemm_persistent_wide<Epi, kEW>;
+  constexpr int threads = wide_threads(kEW);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kWideSmemBytes));
+  if (e != cudaSuccess) return e;
+  int clusters = max_pair_clusters(reinterpret_cast<const void*>(kernel), kEW == 16 ? 2 : 1,
+                                   threads, kWideSmemBytes);
+  if (clusters <= 0) clusters = sms / 2;
+  const int wide_tiles = ((g.tiles_m + 1) / 2) * ((g.tiles_n + 1) / 2);
+  if (clusters > wide_tiles) clusters = wide_tiles;
+  kernel<<<2 * clusters, threads, kWideSmemBytes, st>>>(a, b, g, ea, dev_err);
+  return cudaGetLastError();
+}
+
+// FLCE_WIDE_EPI_WARPS=8 runs every wide epilogue on 8 warps (an A/B switch;
+// by default each epilogue's kWideWarps applies).
+static bool wide_epi_warps_forced_8() {
+  const char* e = std::getenv("FLCE_WIDE_EPI_WARPS");
+  return e && std::atoi(e) == 8;
+}
+
 template <class Epi>
 static cudaError_t launch_wide(const CUtensorMap& a, const CUtensorMap& b, const GemmGeom& g,
                                const typename Epi::Args& ea, int* dev_err, int sms,
                                cudaStream_t st) {
-  auto kernel = gemm_persistent_wide<Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kWideSmemBytes));
-  if (e != cudaSuccess) return e;
-  int clusters = max_pair_clusters(reinterpret_cast<const void*>(kernel), 1, kWideThreads,
-                                   kWideSmemBytes);
-  if (clusters <= 0) clusters = sms / 2;
-  const int wide_tiles = ((g.tiles_m + 1) / 2) * ((g.tiles_n + 1) / 2);
-  if (clusters > wide_tiles) clusters = wide_tiles;
-  kernel<<<2 * clusters, kWideThreads, kWideSmemBytes, st>>>(a, b, g, ea, dev_err);
-  return cudaGetLastError();
+  if constexpr (Epi::kWideWarps == 16) {
+    if (!wide_epi_warps_forced_8())
+      return launch_wide_warps<Epi, 16>(a, b, g, ea, dev_err, sms, st);
+  }
+  return launch_wide_warps<Epi, 8>(a, b, g, ea, dev_err, sms, st);
 }
 
 template <class Epi>

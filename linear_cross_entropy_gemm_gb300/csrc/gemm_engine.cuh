@@ -13,7 +13,7 @@
 // order chosen per problem so the operand shared by concurrent CTAs stays in L2.
 // Two cluster forms follow the single-CTA one: gemm_persistent_pair (two CTAs,
 // cta_group::2, one 256 x 256 tile) and gemm_persistent_wide (two CTAs, one
-// 256 x 512 tile as two MMAs per K step sharing A, 8 epilogue warps).
+// 256 x 512 tile as two MMAs per K step sharing A, 8 or 16 epilogue warps).
 //
 // Operands are 128-byte-swizzled bf16 tiles loaded by TMA, either K-major
 // (rows of 64 contiguous K elements) or MN-major (rows of 64 contiguous M/N
@@ -56,6 +56,35 @@ struct GemmGeom {
   int band_n;             // >0: bands of band_n N-tiles; inside a band N inner, M outer
   int ab_fp16;            // operands are fp16 (else bf16)
 };
+
+// The 32-column chunks of a 128 x 256 accumulator sub-tile that one epilogue
+// warp drains. A warp takes all eight, or (in the 256 x 512 kernel with 16
+// epilogue warps) one half of them while a partner warp of the same TMEM lane
+// quarter takes the other; an epilogue whose row results span the sub-tile
+// then combines them: the second warp publishes its 32 rows' results in xchg
+// and arrives on xbar, the first waits (bounded) and merges.
+struct EpiSlice {
+  int c_lo, c_hi;            // chunks [c_lo, c_hi) of the sub-tile's kBN / 32
+  int sub;                   // -1: the whole sub-tile; 0 / 1: first / second half
+  uint64_t* xbar;            // sub >= 0: barrier of the pair (32 arrivals per phase)
+  float4* xchg;              // sub >= 0: 32 slots, one per row, written by sub 1
+  uint32_t xph;              // parity of xbar's phase for this sub-tile
+  volatile int* abort_flag;  // the CTA's abort flag (for the bounded wait)
+  int* dev_err;
+};
+
+__device__ __forceinline__ EpiSlice whole_slice() {
+  EpiSlice sl;
+  sl.c_lo = 0;
+  sl.c_hi = kBN / 32;
+  sl.sub = -1;
+  sl.xbar = nullptr;
+  sl.xchg = nullptr;
+  sl.xph = 0;
+  sl.abort_flag = nullptr;
+  sl.dev_err = nullptr;
+  return sl;
+}
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& tm, int& tn) {
   if (g.band_m > 0) {
@@ -238,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- epilogue
     const int quad = warp & 3;  // TMEM lane quadrant this warp may access
     const int row_in_tile = quad * 32 + lane;
+    const EpiSlice sl = whole_slice();
     int acc = 0;
     uint32_t aph = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
@@ -247,7 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kBN);
-      Epi::tile(ea, g, tm, tn, row_in_tile, lane, quad, taddr, stage + (warp - 2) * kStageBytes);
+      Epi::tile(ea, g, tm, tn, row_in_tile, lane, quad, taddr, stage + (warp - 2) * kStageBytes,
+                sl);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
       acc ^= 1;
@@ -443,6 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- epilogue (both CTAs)
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
+    const EpiSlice sl = whole_slice();
     const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
     int acc = 0;
     uint32_t aph = 0;
@@ -454,7 +486,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t taddr =
           tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + static_cast<uint32_t>(acc * kBN);
       Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr,
-                stage + (warp - 2) * kStageBytes);
+                stage + (warp - 2) * kStageBytes, sl);
       tc_fence_before();
       mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
       acc ^= 1;
@@ -479,35 +511,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // from L2 into shared memory per flop. The 128 x 512 fp32 accumulator fills
 // all 512 TMEM columns, so there is one accumulator: a tile's epilogue does not
 // overlap the next tile's MMAs (the producer keeps prefetching meanwhile).
-// Eight epilogue warps drain the two 256-column halves at the same time; each
+// The epilogue warps drain the two 256-column halves at the same time; each
 // half is a 128 x 256 sub-tile for the same epilogues as the other forms.
+// kEW = 8 gives each warp a whole sub-tile's rows of one TMEM lane quarter;
+// kEW = 16 splits each sub-tile's columns between two warps of the same lane
+// quarter (4 epilogue warps per SM sub-partition instead of 2: the drain is
+// latency-bound, and it is exposed, since the accumulator fills TMEM).
 //   full[s]  (even CTA) : both CTAs' TMA bytes of stage s
 //   empty[s] (each CTA) : pair MMA commit, multicast to both CTAs
 //   tfull    (each CTA) : pair MMA commit after a tile's last K step
-//   tempty   (even CTA) : 512 epilogue arrivals, 256 from each CTA
+//   tempty   (even CTA) : 2 x 32 kEW epilogue arrivals, one per epilogue thread
+//   xbar[8]  (each CTA) : kEW = 16 only; a column-split warp pair's hand-off
 constexpr int kWideStages = 4;
 constexpr int kWideBHalfBytes = (kBN / 2) * kBK * 2;           // 16 KiB
 constexpr int kWideBStageBytes = 2 * kWideBHalfBytes;          // 32 KiB
-constexpr int kWideThreads = 320;
-constexpr int kWideEpiThreads = 256;
+constexpr int kWideStageRegion = 8 * kStageBytes;  // shared by the epilogue warps
 constexpr size_t kWideSmemBytes =
     1024 + static_cast<size_t>(kWideStages) * (kPairAStageBytes + kWideBStageBytes) +
-    8 * kStageBytes + kBarrierBytes;
+    kWideStageRegion + kBarrierBytes;
+constexpr int wide_threads(int epi_warps) { return 64 + 32 * epi_warps; }
 
-template <class Epi>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
+template <class Epi, int kEW>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide_threads(kEW), 1)
     gemm_persistent_wide(const __grid_constant__ CUtensorMap mapA,
                          const __grid_constant__ CUtensorMap mapB, const GemmGeom g,
                          const __grid_constant__ typename Epi::Args ea, int* dev_err) {
   constexpr bool kAMN = Epi::kAMN;
   constexpr bool kBMN = Epi::kBMN;
+  static_assert(kEW == 8 || kEW == 16, "8 or 16 epilogue warps");
+  constexpr int kWarpStage = kWideStageRegion / kEW;  // staging bytes per epilogue warp
+  static_assert(Epi::kStageNeed <= kWarpStage, "epilogue staging does not fit");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kWideStages * kPairAStageBytes;
-  uint8_t* stage = sB + kWideStages * kWideBStageBytes;  // 8 epilogue warps x kStageBytes
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + 8 * kStageBytes);
+  uint8_t* stage = sB + kWideStages * kWideBStageBytes;  // kEW epilogue warps x kWarpStage
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stage + kWideStageRegion);
   uint64_t* full = bars;
   uint64_t* empty = bars + kWideStages;
   uint64_t* tfull = bars + 2 * kWideStages;
@@ -515,6 +555,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
   uint64_t* done_bar = tempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* xbar = done_bar + 2;  // [2 halves x 4 lane quarters], kEW = 16
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -529,8 +570,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(tfull, 1);
-    mbar_init(tempty, 2 * kWideEpiThreads);
+    mbar_init(tempty, 2 * 32 * kEW);
     mbar_init(done_bar, 1);
+    if constexpr (kEW == 16)
+      for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 32);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -662,12 +705,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
       mbar_drain(done_bar, 0);
     }
   } else {
-    // ------------------------------------------- epilogue (both CTAs, 8 warps)
-    // Warps 2..5 take N half 0, warps 6..9 half 1; warp w reads TMEM lanes
-    // 32 (w % 4) .. 32 (w % 4) + 31.
-    const int half = (warp - 2) >> 2;
+    // ----------------------------------------- epilogue (both CTAs, kEW warps)
+    // Epilogue warp e = warp - 2 takes column slice e / 4 (kEW / 4 slices of
+    // 512 / (kEW / 4) columns: N half, then the sub-tile's first or second 128
+    // columns when kEW = 16) and reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31.
+    // A column-split pair is warps e and e + 4: same lane quarter, same SM
+    // sub-partition; the second warp's staging buffer holds the hand-off.
+    constexpr int kPerHalf = kEW / 8;  // warps per (lane quarter, N half)
+    constexpr int kChunks = (kBN / 32) / kPerHalf;
+    const int e = warp - 2;
+    const int cs = e >> 2;
+    const int half = cs / kPerHalf;
     const int quad = warp & 3;
     const int row_in_tile = quad * 32 + lane;
+    uint8_t* my_stage = stage + e * kWarpStage;
+    EpiSlice sl;
+    sl.sub = kPerHalf == 1 ? -1 : cs % kPerHalf;
+    sl.c_lo = (sl.sub < 0 ? 0 : sl.sub) * kChunks;
+    sl.c_hi = sl.c_lo + kChunks;
+    sl.xbar = &xbar[half * 4 + quad];
+    sl.xchg = reinterpret_cast<float4*>(sl.sub == 0 ? my_stage + 4 * kWarpStage : my_stage);
+    sl.xph = 0;
+    sl.abort_flag = abort_flag;
+    sl.dev_err = dev_err;
     const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
     uint32_t aph = 0;
     for (int t = cluster; t < num_tiles; t += nclusters) {
@@ -681,7 +741,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kWideThreads, 1)
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
                                static_cast<uint32_t>(half * kBN);
         Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr,
-                  stage + (warp - 2) * kStageBytes);
+                  my_stage, sl);
+        sl.xph ^= 1;
       }
       tc_fence_before();
       mbar_arrive_cluster(tempty0);

@@ -1,6 +1,7 @@
-"""GPU parity of both GEMM kernel forms, selected per call through
-flce_params_t.gemm_form (one CTA per 128 x 256 tile, or a CTA pair per
-256 x 256 tile), and of configurations chosen by the autotuner."""
+"""GPU parity of the GEMM kernel forms, selected per call through
+flce_params_t.gemm_form (one CTA per 128 x 256 tile, a CTA pair per
+256 x 256 tile, or a CTA pair per 256 x 512 tile with 8 or 16 epilogue
+warps), and of configurations chosen by the autotuner."""
 import numpy as np
 import pytest
 import torch
@@ -38,6 +39,23 @@ CASES = {
 def test_each_gemm_form_matches_the_oracle(form, case, store):
     wl, kw = CASES[case]
     full_check(wl, store=store, gemm_form=form, **kw)
+
+
+@pytest.mark.parametrize("warps", ["16", "8"])
+def test_wide_epilogue_warp_counts_match_the_oracle(warps, monkeypatch):
+    # The 256 x 512 kernel drains the forward and the bias-free recompute with
+    # 16 epilogue warps, two per (lane quarter, N half) splitting the columns;
+    # FLCE_WIDE_EPI_WARPS=8 gives every epilogue 8. V = 800: the second wide
+    # tile's N half 1 has its first 32 columns in the vocabulary and its second
+    # 128 wholly past V, so one warp of a split pair contributes nothing.
+    if warps == "8":
+        monkeypatch.setenv("FLCE_WIDE_EPI_WARPS", "8")
+    else:
+        monkeypatch.delenv("FLCE_WIDE_EPI_WARPS", raising=False)
+    wl = I.Workload("wide_warps", N=300, H=264, V=800, seed=35, ignore_frac=0.1,
+                    label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.9)
+    full_check(wl, gemm_form="wide", bwd_vocab_block=512)
+    full_check(wl.with_(b_std=0.3, seed=36), gemm_form="wide")
 
 
 def test_forms_compute_the_same_products():
