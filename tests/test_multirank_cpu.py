@@ -1,5 +1,8 @@
-"""Multi-rank host logic on CPU with the gloo backend (world size 2): the
-benchmark's replicas are timed by the slowest rank. No GPU involved."""
+"""Multi-rank host logic on CPU with the gloo backend: the benchmark's
+replicas are timed by the slowest rank; the vocabulary-parallel exchange
+(MAX of m, rescale, SUM of the rest) gives the whole-vocabulary statistics
+over 2 or 3 uneven shards; a rank lost before the exchange makes the
+survivor's collective fail instead of hang. No GPU involved."""
 import os
 import socket
 
@@ -56,6 +59,9 @@ def _stats_of(z):
     return m, d
 
 
+CUTS = {2: [0, 3, 10], 3: [0, 1, 7, 10]}  # uneven shards of V = 10 (one of width 1)
+
+
 def _protocol_worker(rank, world, port, q):
     import numpy as np
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -66,7 +72,7 @@ def _protocol_worker(rank, world, port, q):
         r = np.random.default_rng(5)
         z = r.standard_normal((6, 10)) * 3.0          # the whole-vocabulary logits
         y = np.array([0, 9, 4, 6, 2, 7])
-        cuts = [0, 3, 10]                               # uneven shards of V = 10
+        cuts = CUTS[world]
         a, b = cuts[rank], cuts[rank + 1]
         zl = z[:, a:b]
         m, d = _stats_of(zl)
@@ -89,9 +95,9 @@ def _protocol_worker(rank, world, port, q):
         dist.destroy_process_group()
 
 
-def test_vocab_parallel_exchange_protocol_two_ranks():
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_parallel_exchange_protocol(world):
     import numpy as np
-    world = 2
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
@@ -106,3 +112,48 @@ def test_vocab_parallel_exchange_protocol_two_ranks():
         np.testing.assert_allclose(lse, ref_lse, rtol=1e-13)
         np.testing.assert_allclose(zy, ref_zy, rtol=1e-15)
         np.testing.assert_allclose(sz, ref_sz, rtol=1e-13)
+
+
+def _dying_rank_worker(rank, world, port, q):
+    import datetime
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world,
+                            timeout=datetime.timedelta(seconds=10))
+    if rank == 1:
+        os._exit(3)  # leaves between steps, before its exchange
+    from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
+    stats = torch.ones(4, 6, dtype=torch.float64)
+
+    def gloo_allreduce(t, op):
+        dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+
+    def cpu_rescale(s, gmax):
+        s[1] *= torch.exp2(s[0] - gmax)
+        s[0] = gmax
+
+    try:
+        VP.merge_stats(stats, gloo_allreduce, cpu_rescale)
+        q.put((rank, "returned"))
+    except Exception as e:  # the collective reports the lost peer
+        q.put((rank, "raised " + type(e).__name__))
+    os._exit(0)
+
+
+def test_vocab_parallel_exchange_reports_a_lost_rank():
+    # A rank that exits before the exchange: the survivor's first all-reduce
+    # ends with an error (peer gone, or the 10 s process-group timeout), it
+    # does not hang and does not return merged statistics.
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dying_rank_worker, args=(r, world, port, q))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(90)
+    assert all(p.exitcode is not None for p in procs), "a rank hung"
+    assert procs[1].exitcode == 3
+    rank, what = q.get(timeout=10)
+    assert rank == 0 and what.startswith("raised"), what
