@@ -66,7 +66,7 @@ typedef enum {
   FLCE_ERR_UNSUPPORTED = 7        /* device is not sm_103 / sizes beyond the int32 tile grid */
 } flce_status_t;
 
-/* GEMM kernel form of a call (flce_params_t.gemm_form). Both forms compute
+/* GEMM kernel form of a call (flce_params_t.gemm_form). All forms compute
  * the same products; results differ only in the order of fp32 accumulation
  * inside a tile, not in what is summed. */
 typedef enum {
