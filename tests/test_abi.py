@@ -38,6 +38,26 @@ def test_library_exports_every_declared_symbol(lib):
     assert not missing, f"not exported: {missing}"
 
 
+def _enum(prefix):
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {m.group(1): int(m.group(2))
+            for m in re.finditer(prefix + r"([A-Z0-9_]+)\s*=\s*(\d+)", src)}
+
+
+def test_binding_codes_match_the_header_enums():
+    # Trace kinds (the binding's names index flce_kernel_t), GEMM forms and
+    # reductions: the Python side must use the header's values.
+    kinds = _enum("FLCE_KERNEL_")
+    assert [k.lower() for k, _ in sorted(kinds.items(), key=lambda kv: kv[1])] == \
+        list(_lib.KERNEL_NAMES)
+    assert sorted(kinds.values()) == list(range(len(kinds)))
+    forms = _enum("FLCE_GEMM_")
+    assert {"default": forms["DEFAULT"], "single": forms["SINGLE_CTA"],
+            "pair": forms["CTA_PAIR"], "wide": forms["WIDE_PAIR"]} == _lib.GEMM_FORMS
+    red = _enum("FLCE_REDUCTION_")
+    assert {k.lower(): v for k, v in red.items()} == _lib.REDUCTION
+
+
 def test_params_struct_layout_matches_header():
     assert ctypes.sizeof(_lib.FlceParams) == 96
     assert _lib.FlceParams.bwd_vocab_block.offset == 64
