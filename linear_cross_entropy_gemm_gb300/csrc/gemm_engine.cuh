@@ -1,7 +1,7 @@
 // Persistent, warp-specialised tcgen05 GEMM engine shared by every
 // contraction of the fused linear cross-entropy (FLCE) path.
 //
-//   D[M, N] = A[M, K] * B[N, K]^T   (bf16 in, fp32 accumulate in TMEM)
+//   D[M, N] = A[M, K] * B[N, K]^T   (bf16 or fp16 in, fp32 accumulate in TMEM)
 //
 // One CTA per SM (192 threads):
 //   warp 0      TMA producer: a kStages-deep ring of (A, B) K-slices in smem
@@ -15,7 +15,7 @@
 // cta_group::2, one 256 x 256 tile) and gemm_persistent_wide (two CTAs, one
 // 256 x 512 tile as two MMAs per K step sharing A, 8 or 16 epilogue warps).
 //
-// Operands are 128-byte-swizzled bf16 tiles loaded by TMA, either K-major
+// Operands are 128-byte-swizzled 16-bit tiles loaded by TMA, either K-major
 // (rows of 64 contiguous K elements) or MN-major (rows of 64 contiguous M/N
 // elements, one per K index); the tcgen05 instruction descriptor's transpose
 // bits select the form, so dW = dL^T x and dx = dL W need no transposed copies.
