@@ -136,8 +136,11 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     fp32 (none); lse is [N] fp32. Runs on the current stream, no sync.
     With ``saved`` (a uint8 CUDA tensor of flce_saved_size bytes) the forward
     also keeps the state the stored-probability backward needs.
-    ``gemm_form``: "default", "single" (128 x 256 CTA tiles) or "pair"
-    (256 x 256 tiles on CTA pairs); see ``tuning.autotune``."""
+    ``gemm_form``: "default", "single" (128 x 256 CTA tiles), "pair"
+    (256 x 256 tiles on CTA pairs) or "wide" (256 x 512 tiles on CTA pairs);
+    see ``tuning.autotune``. ``workspace``: a uint8 CUDA tensor of at least
+    flce_workspace_size(..., "forward") bytes; when it is not given, or is
+    smaller, a new one is allocated for the call."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
@@ -182,7 +185,8 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
     With ``saved`` (filled by flce_forward(..., saved=)) the logits are not
     recomputed: dlogits come from the stored tile probabilities.
     ``bwd_vocab_block`` (0 = library default) and ``gemm_form`` select the
-    vocabulary block and GEMM form; see ``tuning.autotune``."""
+    vocabulary block and GEMM form; see ``tuning.autotune``. ``workspace``: as
+    in flce_forward, with flce_workspace_size(..., "backward") bytes."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
