@@ -395,7 +395,7 @@ flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const vo
 
 size_t flce_saved_size(const flce_params_t* p) {
   if (check_params(p) != FLCE_OK || p->N == 0) return 0;
-  Saved sv;
+  Saved sv{};  // filled by carve_saved when `saved` is given
   return carve_saved(p, nullptr, &sv);
 }
 
@@ -430,7 +430,7 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   FwdWs w;
   const size_t need = carve_fwd(p, nullptr, &w);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  Saved sv;
+  Saved sv{};  // filled by carve_saved when `saved` is given
   if (saved) {
     if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
@@ -592,7 +592,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
   BwdWs w;
   const size_t need = carve_bwd(p, nullptr, &w);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  Saved sv;
+  Saved sv{};  // filled by carve_saved when `saved` is given
   if (saved) {
     if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
