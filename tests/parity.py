@@ -99,5 +99,36 @@ def assert_grad_close(got, ref, what):
         f"(<= {GRAD_MAX * mref:.3e})"
 
 
+def token_seams(N: int) -> list:
+    """Token rows at the seams the kernels' tilings have at N tokens: the
+    128-row tile, the 256-row CTA pair, the 4096-row band of the logits
+    GEMMs' raster, and the last (possibly partial) tiles."""
+    rows = {0, 1, N - 1, N - 2}
+    for period in (128, 256, 4096):
+        for k in range(period, N, period):
+            if k in (period, 2 * period) or k >= N - 2 * period:
+                rows.update((k - 1, k))
+    if N > 256:
+        rows.update((N - 257, N - 256, N - 129, N - 128))
+        last = (N - 1) // 256 * 256
+        rows.update((last - 1, last))
+    return sorted(r for r in rows if 0 <= r < N)
+
+
+def vocab_seams(V: int, block: int) -> list:
+    """Vocabulary rows at the seams of the backward's vocabulary blocks (each
+    block start -1, +0, +1), of the 256- and 512-column GEMM tiles near the
+    start, and of the last tiles and block."""
+    cols = {0, 1, 255, 256, 257, 511, 512, 513, V - 1, V - 2}
+    for v0 in range(block, V, block):
+        cols.update((v0 - 1, v0, v0 + 1))
+    for period in (256, 512):
+        last = (V - 1) // period * period
+        cols.update((last - 1, last))
+    last_block = (V - 1) // block * block
+    cols.update((last_block, last_block + 1))
+    return sorted(c for c in cols if 0 <= c < V)
+
+
 def to_np(t):
     return None if t is None else t.detach().float().cpu().numpy()

@@ -12,7 +12,9 @@ import torch
 import linear_cross_entropy_gemm_gb300 as F
 from linear_cross_entropy_gemm_gb300 import inputs as I
 from oracle import flce_oracle as O
-from parity import (DeviceProblem, assert_grad_close, assert_loss_close, f64, opts_of, to_np)
+from linear_cross_entropy_gemm_gb300 import tuning
+from parity import (DeviceProblem, assert_grad_close, assert_loss_close, f64, opts_of, to_np,
+                    token_seams, vocab_seams)
 
 pytestmark = pytest.mark.gpu
 
@@ -235,12 +237,19 @@ def _sampled(name):
     tl = O.token_losses_from_stats(lse, zt, sz, inp.y, wl.V, wl.ignore_index,
                                    wl.label_smoothing, wl.lse_square_scale)
     ref_loss = O.reduce_losses(tl, inp.y, wl.ignore_index, wl.reduction)
+    # Forced samples: the seams of the tilings and of the backward vocabulary
+    # block the library picks by default at this size (parity.token_seams,
+    # parity.vocab_seams), ignored tokens, and the most frequent targets.
     ignored = np.nonzero(inp.y == wl.ignore_index)[0][:8]
-    rows = I.sample_indices(wl.seed, wl.N, 256, must_include=list(ignored) + [0, wl.N - 1])
+    rows = I.sample_indices(wl.seed, wl.N, 256,
+                            must_include=list(ignored) + token_seams(wl.N))
     valid_y = inp.y[inp.y != wl.ignore_index]
     top = np.argsort(-np.bincount(valid_y, minlength=wl.V))[:8] if valid_y.size else []
-    edges = [0, 1, 255, 256, 16383, 16384, wl.V - 256, wl.V - 1]
-    vrows = I.sample_indices(wl.seed + 1, wl.V, 256, must_include=list(top) + edges)
+    block = tuning.library_default_block(wl.N, wl.V)
+    vrows = I.sample_indices(wl.seed + 1, wl.V, 256,
+                             must_include=list(top) + vocab_seams(wl.V, block))
+    assert set(token_seams(wl.N)) <= set(rows.tolist())
+    assert set(vocab_seams(wl.V, block)) <= set(vrows.tolist())
     dl = inp.dloss.astype(np.float64)
     rdx = O.dx_rows(rows, dl, x64, W64, b64, inp.y, **opts)
     rdW, rdb = O.dW_db_rows(vrows, lse, dl, x64, W64, b64, inp.y, **opts)

@@ -105,3 +105,25 @@ def test_tune_result_serialises():
                           {("pair", 65536): 2.0}, key=("dev",))
     d = r.as_dict()
     assert d["config"]["bwd_vocab_block"] == 65536 and d["backward_ms"] == {"pair/65536": 2.0}
+
+
+@pytest.mark.parametrize("name", ["llama3_head", "large_logit", "vocab256k"])
+def test_full_size_samples_cover_the_default_seams(name):
+    # The full-size parity samples force the rows at every seam of the
+    # default backward vocabulary block and of the tilings (host logic only).
+    import sys, os
+    sys.path.insert(0, os.path.dirname(__file__))
+    from parity import token_seams, vocab_seams
+    from linear_cross_entropy_gemm_gb300 import inputs as I
+    wl = I.WORKLOADS[name]
+    bv = tuning.library_default_block(wl.N, wl.V)
+    cols = set(vocab_seams(wl.V, bv))
+    for v0 in range(bv, wl.V, bv):
+        assert {v0 - 1, v0, v0 + 1} <= cols
+    assert {511, 512, wl.V - 1} <= cols
+    rows = set(token_seams(wl.N))
+    assert {255, 256, 511, 512, 4095, 4096, wl.N - 256, wl.N - 1} <= rows
+    rows_s = I.sample_indices(wl.seed, wl.N, 256, must_include=sorted(rows))
+    cols_s = I.sample_indices(wl.seed + 1, wl.V, 256, must_include=sorted(cols))
+    assert len(rows_s) == 256 and len(cols_s) == 256
+    assert rows <= set(rows_s.tolist()) and cols <= set(cols_s.tolist())
