@@ -116,7 +116,8 @@ typedef enum {
   FLCE_KERNEL_BWD_DLOGITS = 4,  /* recompute a vocab block's logits -> bf16 dL */
   FLCE_KERNEL_BWD_DB = 5,       /* bias-gradient partial sum of a block */
   FLCE_KERNEL_BWD_DW = 6,       /* dW block GEMM */
-  FLCE_KERNEL_BWD_DX = 7        /* dx accumulate GEMM */
+  FLCE_KERNEL_BWD_DX = 7,       /* dx accumulate GEMM */
+  FLCE_KERNEL_BWD_CONVERT = 8   /* stored or kept probabilities -> dL (an HBM pass) */
 } flce_kernel_t;
 
 /* Optional per-kernel timing without a profiler. The caller creates
@@ -133,8 +134,10 @@ typedef struct {
   int32_t* kinds;
 } flce_trace_t;
 
-/* Workspace bytes a call needs: which = 0 for flce_forward, 1 for
- * flce_backward. Returns 0 for invalid parameters or N == 0. */
+/* Workspace bytes a call needs: which = 0 for the forward calls, 1 for
+ * flce_backward (and the stored and shard backwards), 2 for
+ * flce_backward_keep (no dL block: it stages dL in the kept buffer).
+ * Returns 0 for invalid parameters or N == 0. */
 size_t flce_workspace_size(const flce_params_t* p, int which);
 
 /* The GEMM form (FLCE_GEMM_SINGLE_CTA, _CTA_PAIR or _WIDE_PAIR) that calls with
@@ -207,6 +210,44 @@ flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss, co
                                   const void* W, const void* b, const int64_t* y, void* dx,
                                   void* dW, void* db, void* workspace, size_t workspace_bytes,
                                   int32_t* dev_err, void* stream, flce_trace_t* trace);
+
+/*
+ * Kept-block mode: the backward recomputes every vocabulary block but the
+ * first. (Our combination of DeepSpeed PR #8792 "What", where the backward
+ * recomputes the logits one vocabulary block at a time into a staged block,
+ * with the grad-in-forward of Liger-Kernel commit 95b01e9, which forms the
+ * gradient from logits the forward already holds.)
+ *
+ * flce_forward_keep computes what flce_forward does and also leaves, in the
+ * caller's `kept` buffer (flce_kept_size(p) bytes, 16-byte aligned), the
+ * probabilities of the first backward vocabulary block [0, BVc), where BVc is
+ * the block flce_backward would use for p (bwd_vocab_block, or the library
+ * default): each 32-column chunk's q = exp(z - m_c) as fp16 in an [N, BVc]
+ * array, m_c being the running maximum of the row's logits up to that chunk,
+ * plus the m_c (fp32). These are exponentials the forward's online softmax
+ * computes anyway. flce_backward_keep turns that block into its dlogits in
+ * place (an HBM pass instead of 2 N H BVc flops of recompute) and then uses
+ * the same buffer as the dL staging block of the blocks it recomputes, so
+ * its workspace (flce_workspace_size(p, 2)) holds no dL block: the kept
+ * buffer plus that workspace take the same memory as flce_backward's
+ * workspace. At the Llama-3 head shape (V = 128256, BVc = 65536) this skips
+ * half of the recompute, an eighth of the step's flops.
+ * Both calls take the same p (the kept layout depends on N, V and BVc); the
+ * backward consumes the kept state (it holds dL afterwards), and the buffer
+ * must be left untouched between the two calls. Plain (whole-vocabulary)
+ * calls only; trace may be NULL.
+ */
+size_t flce_kept_size(const flce_params_t* p);
+flce_status_t flce_forward_keep(const flce_params_t* p, const void* x, const void* W,
+                                const void* b, const int64_t* y, float* loss, float* lse,
+                                void* kept, size_t kept_bytes, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                flce_trace_t* trace);
+flce_status_t flce_backward_keep(const flce_params_t* p, const float* dloss, const float* lse,
+                                 void* kept, size_t kept_bytes, const void* x, const void* W,
+                                 const void* b, const int64_t* y, void* dx, void* dW, void* db,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                 void* stream, flce_trace_t* trace);
 
 /*
  * Vocabulary-parallel FLCE (DeepSpeed PR #8792, "What": each rank holds a

@@ -27,7 +27,7 @@ __all__ = [
     "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
     "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
     "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace", "flce_saved_size",
-    "GEMM_FORMS", "resolved_gemm_form",
+    "GEMM_FORMS", "resolved_gemm_form", "flce_kept_size",
 ]
 
 _err_words = {}
@@ -99,8 +99,11 @@ class KernelTrace:
 
 
 def flce_workspace_size(N, H, V, which: str, **opts) -> int:
+    """Workspace bytes of a call: which = "forward", "backward" or
+    "backward_keep" (the backward of a kept-block forward, which stages dL in
+    the kept buffer and so needs no dL block of its own)."""
     p = params(N, H, V, **opts)
-    return int(_lib.load().flce_workspace_size(p, 0 if which == "forward" else 1))
+    return int(_lib.load().flce_workspace_size(p, _lib.WORKSPACE_KIND[which]))
 
 
 GEMMS = ("fwd_lse", "bwd_dlogits", "bwd_dw", "bwd_dx")
@@ -124,6 +127,15 @@ def flce_saved_size(N, H, V, **opts) -> int:
     return int(_lib.load().flce_saved_size(params(N, H, V, **opts)))
 
 
+def flce_kept_size(N, H, V, **opts) -> int:
+    """Bytes of the state flce_forward(..., kept=) leaves for the backward: the
+    first backward vocabulary block's fp16 probabilities [N, BVc] and the
+    running maxima of its 32-column chunks. It doubles as the backward's dL
+    staging block, so a kept-block forward + backward takes no more memory
+    than the plain pair."""
+    return int(_lib.load().flce_kept_size(params(N, H, V, **opts)))
+
+
 def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: torch.Tensor, *,
                  ignore_index: int = -100, label_smoothing: float = 0.0,
                  lse_square_scale: float = 0.0, logit_scale: float = 1.0,
@@ -131,7 +143,8 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
                  out: Optional[Tuple[torch.Tensor, torch.Tensor]] = None,
                  stream=None, trace: Optional[KernelTrace] = None,
                  saved: Optional[torch.Tensor] = None,
-                 gemm_form="default") -> Tuple[torch.Tensor, torch.Tensor]:
+                 gemm_form="default", kept: Optional[torch.Tensor] = None,
+                 bwd_vocab_block: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss and per-token lse. loss is a 0-dim fp32 tensor (sum/mean) or [N]
     fp32 (none); lse is [N] fp32. Runs on the current stream, no sync.
     With ``saved`` (a uint8 CUDA tensor of flce_saved_size bytes) the forward
@@ -140,15 +153,22 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     (256 x 256 tiles on CTA pairs) or "wide" (256 x 512 tiles on CTA pairs);
     see ``tuning.autotune``. ``workspace``: a uint8 CUDA tensor of at least
     flce_workspace_size(..., "forward") bytes; when it is not given, or is
-    smaller, a new one is allocated for the call."""
+    smaller, a new one is allocated for the call.
+    With ``kept`` (a uint8 CUDA tensor of flce_kept_size bytes; give the
+    backward's ``bwd_vocab_block`` here too) the forward also leaves the first
+    backward vocabulary block's probabilities for flce_backward(..., kept=),
+    which then skips that block's recompute."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
     V = W.shape[0]
+    if saved is not None and kept is not None:
+        raise ValueError("flce: give saved= or kept=, not both")
     p = params(N, H, V, ignore_index=ignore_index, label_smoothing=label_smoothing,
                lse_square_scale=lse_square_scale, logit_scale=logit_scale,
                reduction=reduction, has_bias=b is not None,
-               input_fp16=x.dtype == torch.float16, gemm_form=gemm_form)
+               input_fp16=x.dtype == torch.float16, gemm_form=gemm_form,
+               bwd_vocab_block=bwd_vocab_block)
     dev = x.device
     if out is not None:
         loss, lse = out
@@ -158,12 +178,13 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     need = lib.flce_workspace_size(p, 0)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    if saved is not None:
-        _check_saved(saved, lib, p)
-        st = lib.flce_forward_store(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse),
-                                    _ptr(saved), saved.numel(), _ptr(workspace), workspace.numel(),
-                                    _ptr(device_error_word(dev)), _stream(stream),
-                                    None if trace is None else trace.struct)
+    if saved is not None or kept is not None:
+        state = saved if saved is not None else kept
+        _check_state(state, lib, p, kept is not None)
+        fn = lib.flce_forward_store if saved is not None else lib.flce_forward_keep
+        st = fn(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse), _ptr(state),
+                state.numel(), _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
+                _stream(stream), None if trace is None else trace.struct)
     else:
         args = (p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(loss), _ptr(lse), _ptr(workspace),
                 workspace.numel(), _ptr(device_error_word(dev)), _stream(stream))
@@ -180,10 +201,15 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                   dW_dtype: torch.dtype = torch.float32, db_dtype: torch.dtype = torch.float32,
                   bwd_vocab_block: int = 0, workspace: Optional[torch.Tensor] = None,
                   out: Optional[Tuple] = None, stream=None, trace: Optional[KernelTrace] = None,
-                  saved: Optional[torch.Tensor] = None, gemm_form="default"):
+                  saved: Optional[torch.Tensor] = None, gemm_form="default",
+                  kept: Optional[torch.Tensor] = None):
     """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None.
     With ``saved`` (filled by flce_forward(..., saved=)) the logits are not
-    recomputed: dlogits come from the stored tile probabilities.
+    recomputed: dlogits come from the stored tile probabilities. With
+    ``kept`` (filled by flce_forward(..., kept=) with the same options and
+    ``bwd_vocab_block``) the first vocabulary block's dlogits come from the
+    kept probabilities and the buffer stages every block's dL; the call
+    consumes it.
     ``bwd_vocab_block`` (0 = library default) and ``gemm_form`` select the
     vocabulary block and GEMM form; see ``tuning.autotune``. ``workspace``: as
     in flce_forward, with flce_workspace_size(..., "backward") bytes."""
@@ -213,16 +239,19 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
         dx = torch.empty(N, H, dtype=x.dtype, device=dev)
         dW = torch.empty(V, H, dtype=dW_dtype, device=dev)
         db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
-    need = lib.flce_workspace_size(p, 1)
+    if saved is not None and kept is not None:
+        raise ValueError("flce: give saved= or kept=, not both")
+    need = lib.flce_workspace_size(p, 2 if kept is not None else 1)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-    if saved is not None:
-        _check_saved(saved, lib, p)
-        st = lib.flce_backward_store(p, _ptr(dloss), _ptr(lse), _ptr(saved), saved.numel(), _ptr(x),
-                                     _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW), _ptr(db),
-                                     _ptr(workspace), workspace.numel(),
-                                     _ptr(device_error_word(dev)), _stream(stream),
-                                     None if trace is None else trace.struct)
+    if saved is not None or kept is not None:
+        state = saved if saved is not None else kept
+        _check_state(state, lib, p, kept is not None)
+        fn = lib.flce_backward_store if saved is not None else lib.flce_backward_keep
+        st = fn(p, _ptr(dloss), _ptr(lse), _ptr(state), state.numel(), _ptr(x), _ptr(W), _ptr(b),
+                _ptr(y), _ptr(dx), _ptr(dW), _ptr(db), _ptr(workspace), workspace.numel(),
+                _ptr(device_error_word(dev)), _stream(stream),
+                None if trace is None else trace.struct)
     else:
         args = (p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW),
                 _ptr(db), _ptr(workspace), workspace.numel(), _ptr(device_error_word(dev)),
@@ -233,11 +262,13 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
     return dx, dW, db
 
 
-def _check_saved(saved, lib, p):
-    if saved.dtype != torch.uint8 or not saved.is_cuda or not saved.is_contiguous():
-        raise TypeError("flce: saved must be a contiguous uint8 CUDA tensor")
-    if saved.numel() < lib.flce_saved_size(p):
-        raise ValueError("flce: saved is smaller than flce_saved_size()")
+def _check_state(state, lib, p, kept: bool):
+    what = "kept" if kept else "saved"
+    if state.dtype != torch.uint8 or not state.is_cuda or not state.is_contiguous():
+        raise TypeError(f"flce: {what} must be a contiguous uint8 CUDA tensor")
+    need = lib.flce_kept_size(p) if kept else lib.flce_saved_size(p)
+    if state.numel() < need:
+        raise ValueError(f"flce: {what} is smaller than flce_{what}_size()")
 
 
 def flce_read_device_error(device=None, stream=None) -> int:
@@ -254,25 +285,36 @@ def flce_read_device_error(device=None, stream=None) -> int:
 
 
 class FusedLinearCrossEntropyFunction(torch.autograd.Function):
-    """Autograd wrapper: forward keeps only lse; backward recomputes the logits."""
+    """Autograd wrapper. By default the forward keeps lse and the first
+    backward vocabulary block's probabilities (the buffer the backward stages
+    dL in, so no extra memory) and the backward recomputes the other blocks'
+    logits; keep_block=False recomputes every block; recompute=False keeps
+    every logit's probability (~2 N V bytes) and recomputes none."""
 
     @staticmethod
     def forward(ctx, x, target, weight, bias=None, ignore_index=-100, label_smoothing=0.0,
                 lse_square_scale=0.0, logit_scale=1.0, reduction="mean", recompute=True,
-                config=None):
-        saved = None
+                config=None, keep_block=True):
+        saved = kept = None
+        N, H, V = x.shape[0], x.shape[1], weight.shape[0]
+        bwd_kw = {} if config is None else config.backward_kwargs()
         if not recompute:
-            n = flce_saved_size(x.shape[0], x.shape[1], weight.shape[0],
-                                label_smoothing=label_smoothing,
+            n = flce_saved_size(N, H, V, label_smoothing=label_smoothing,
                                 input_fp16=x.dtype == torch.float16)
             saved = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
+        elif keep_block and N > 0:
+            n = flce_kept_size(N, H, V, input_fp16=x.dtype == torch.float16,
+                               bwd_vocab_block=bwd_kw.get("bwd_vocab_block", 0))
+            kept = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
         ctx.config = config
         loss, lse = flce_forward(x, weight, bias, target, ignore_index=ignore_index,
                                  label_smoothing=label_smoothing,
                                  lse_square_scale=lse_square_scale, logit_scale=logit_scale,
-                                 reduction=reduction, saved=saved,
+                                 reduction=reduction, saved=saved, kept=kept,
+                                 bwd_vocab_block=bwd_kw.get("bwd_vocab_block", 0),
                                  **({} if config is None else config.forward_kwargs()))
         ctx.saved_state = saved
+        ctx.kept_state = kept
         ctx.save_for_backward(x, target, weight, bias, lse)
         ctx.opts = dict(ignore_index=ignore_index, label_smoothing=label_smoothing,
                         lse_square_scale=lse_square_scale, logit_scale=logit_scale,
@@ -284,32 +326,38 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
         x, target, weight, bias, lse = ctx.saved_tensors
         dx, dW, db = flce_backward(dloss.float().contiguous(), lse, x, weight, bias, target,
                                    dW_dtype=torch.float32, db_dtype=torch.float32,
-                                   saved=ctx.saved_state, **ctx.opts,
+                                   saved=ctx.saved_state, kept=ctx.kept_state, **ctx.opts,
                                    **({} if ctx.config is None else ctx.config.backward_kwargs()))
-        ctx.saved_state = None
+        ctx.saved_state = ctx.kept_state = None
         dW = dW.to(weight.dtype)
         db = None if db is None else db.to(bias.dtype)
-        return dx, None, dW, db, None, None, None, None, None, None, None
+        return dx, None, dW, db, None, None, None, None, None, None, None, None
 
 
 def fused_linear_cross_entropy(x, target, weight, bias=None, ignore_index=-100,
                                label_smoothing=0.0, lse_square_scale=0.0, logit_scale=1.0,
-                               reduction="mean", recompute=True, config=None):
+                               reduction="mean", recompute=True, config=None,
+                               keep_block=True):
     """Functional form; x [N, H] bf16, target [N] int64, weight [V, H] bf16.
-    recompute=False keeps fp16 tile probabilities (~2 N V bytes) from the
-    forward so the backward skips the logits GEMM. ``config``: a
-    ``tuning.FlceConfig`` (GEMM forms, backward vocabulary block), or None for
-    the library defaults."""
+    By default the forward keeps the first backward vocabulary block's
+    probabilities in the buffer the backward stages dL in (no extra memory),
+    so the backward recomputes the logits of the other blocks only;
+    keep_block=False recomputes all. recompute=False keeps fp16 tile
+    probabilities of every logit (~2 N V bytes) so the backward skips the
+    logits GEMM. ``config``: a ``tuning.FlceConfig`` (GEMM forms, backward
+    vocabulary block), or None for the library defaults."""
     return FusedLinearCrossEntropyFunction.apply(x, target, weight, bias, ignore_index,
                                                  label_smoothing, lse_square_scale,
-                                                 logit_scale, reduction, recompute, config)
+                                                 logit_scale, reduction, recompute, config,
+                                                 keep_block)
 
 
 class FusedLinearCrossEntropyLoss(torch.nn.Module):
     """Module form: flattens x [..., H] and target [...] to [N, H] and [N]."""
 
     def __init__(self, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
-                 logit_scale=1.0, reduction="mean", recompute=True, autotune=False):
+                 logit_scale=1.0, reduction="mean", recompute=True, autotune=False,
+                 keep_block=True):
         """autotune=True: the first call for each (shape, dtype, options) key
         times the GEMM forms and backward vocabulary blocks on the caller's
         tensors (tuning.autotune) and later calls reuse the fastest."""
@@ -323,6 +371,7 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         self.reduction = reduction
         self.recompute = recompute
         self.autotune = autotune
+        self.keep_block = keep_block
 
     def forward(self, x, target, weight, bias=None):
         x2 = x.reshape(-1, x.shape[-1]).contiguous()
@@ -337,4 +386,5 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
                 reduction=self.reduction).config
         return fused_linear_cross_entropy(
             x2, y2, weight, bias, self.ignore_index, self.label_smoothing,
-            self.lse_square_scale, self.logit_scale, self.reduction, self.recompute, config)
+            self.lse_square_scale, self.logit_scale, self.reduction, self.recompute, config,
+            self.keep_block)

@@ -57,7 +57,9 @@ class FlceTrace(ctypes.Structure):
 
 
 KERNEL_NAMES = ("fwd_lse", "fwd_merge", "fwd_finalize", "bwd_prep", "bwd_dlogits", "bwd_db",
-                "bwd_dw", "bwd_dx")
+                "bwd_dw", "bwd_dx", "bwd_convert")
+# flce_workspace_size's `which`.
+WORKSPACE_KIND = {"forward": 0, "backward": 1, "backward_keep": 2}
 
 
 class FlceError(RuntimeError):
@@ -100,6 +102,12 @@ def load() -> ctypes.CDLL:
     lib.flce_backward_store.argtypes = [P, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                         vp, vp, T]
     lib.flce_backward_store.restype = ctypes.c_int
+    lib.flce_kept_size.argtypes = [P]
+    lib.flce_kept_size.restype = sz
+    lib.flce_forward_keep.argtypes = lib.flce_forward_store.argtypes
+    lib.flce_forward_keep.restype = ctypes.c_int
+    lib.flce_backward_keep.argtypes = lib.flce_backward_store.argtypes
+    lib.flce_backward_keep.restype = ctypes.c_int
     lib.flce_forward_shard.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.flce_forward_shard.restype = ctypes.c_int
     lib.flce_shard_rescale.argtypes = [P, vp, vp, vp]

@@ -188,6 +188,14 @@ __device__ __forceinline__ void tma_block_16(const CUtensorMap* map, int x, int 
 // Folds each logits tile into per-(row, vocab tile) base-2 online-softmax
 // partials (m = max z log2e, d = sum 2^(z log2e - m)), the tile's sum of z
 // (label smoothing only) and the target logit z_y when y falls in the tile.
+//
+// KEEP (the kept-block forward): every 32-column chunk of the vocabulary
+// columns [0, keep_cols) also leaves its probabilities relative to the running
+// maximum after that chunk, q = 2^(z log2e - m_c) in (0, 1], as fp16 in the
+// kept buffer (a TMA-stored [Ntok, keep_cols] view; these are the exponentials
+// the online softmax computes anyway), and m_c in keep_max[chunk, row]. The
+// backward turns them into that block's dL in place:
+// p = q 2^(m_c - lse log2e).
 struct FwdLseArgs {
   const uint16_t* bias;  // bf16 or fp16 bits
   int fp16;
@@ -200,15 +208,21 @@ struct FwdLseArgs {
   float* part_d;  // [tiles_v, Ntok]
   float* part_s;  // [tiles_v, Ntok] or null
   float* zy;      // [Ntok]
+  int keep_cols;         // KEEP: vocabulary columns kept (<= V)
+  float* keep_max;       // KEEP: [ceil(keep_cols / 32), Ntok]
+  CUtensorMap keep_map;  // KEEP: store map of the kept q, [Ntok, keep_cols] 16-bit
 };
 
-template <bool HAS_BIAS, bool HAS_SMOOTH>
+template <bool HAS_BIAS, bool HAS_SMOOTH, bool KEEP = false>
 struct FwdLseEpi {
   static constexpr bool kAMN = false, kBMN = false;
-  static constexpr int kWideWarps = 16, kStageNeed = 0;
+  // With a bias and without smoothing, the kept variant spills at 16 warps.
+  static constexpr int kWideWarps = (KEEP && HAS_BIAS && !HAS_SMOOTH) ? 8 : 16;
+  static constexpr int kStageNeed = KEEP ? 32 * 32 * 2 : 0;  // one 16-bit 32 x 32 box
   using Args = FwdLseArgs;
   __device__ static void tile(const Args& a, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int lane, int, uint32_t taddr, void*, const EpiSlice& sl) {
+                              int lane, int quad, uint32_t taddr, void* stage,
+                              const EpiSlice& sl) {
     const int row = tm * kBM + row_in_tile;
     const int v0 = tn * kBN;
     const int64_t yv = row < a.Ntok ? __ldg(a.y + row) - a.y_off : -1;
@@ -259,11 +273,24 @@ struct FwdLseEpi {
           acc += tree_sum32(v);
         } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            acc += (col0 + j < a.V) ? fast_exp2(fmaf(v[j], c2, -nm)) : 0.f;
+          for (int j = 0; j < 32; ++j) {
+            const float q = (col0 + j < a.V) ? fast_exp2(fmaf(v[j], c2, -nm)) : 0.f;
+            if constexpr (KEEP) v[j] = q;
+            acc += q;
+          }
         }
         d = acc;
         m = nm;
+      }
+      if constexpr (KEEP) {
+        // col0 < keep_cols <= V: the chunk has a real column, so nm is finite
+        // and v holds its q. The map clips rows past Ntok and columns past
+        // keep_cols. (The same for the whole warp.)
+        if (col0 < a.keep_cols) {
+          const int row0 = tm * kBM + quad * 32;
+          if (row0 < a.Ntok) tma_block_16(&a.keep_map, col0, row0, v, true, stage, lane);
+          if (row < a.Ntok) a.keep_max[static_cast<size_t>(col0 >> 5) * a.Ntok + row] = nm;
+        }
       }
     }
     // The target column lies in at most one warp's chunks.
@@ -271,6 +298,12 @@ struct FwdLseEpi {
     if (row < a.Ntok && has_t) a.zy[row] = ut * a.scale;
     if (sl.sub == 1) {
       // Second half of a column-split sub-tile: hand (m, d, S) to the partner.
+      // The hand-off slots are this warp's staging buffer: with KEEP, its last
+      // q box must have been read out by the TMA engine first.
+      if constexpr (KEEP) {
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+      }
       sl.xchg[lane] = make_float4(m, d, S, 0.f);
       mbar_arrive(sl.xbar);
       return;

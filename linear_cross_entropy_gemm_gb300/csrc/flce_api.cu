@@ -230,14 +230,16 @@ struct BwdWs {
   float* dl_scale;   // [2]
 };
 
-size_t carve_bwd(const flce_params_t* p, void* base, BwdWs* w) {
+// kept: the backward of a kept-block forward stages dL in the kept buffer,
+// so its workspace holds no dL block.
+size_t carve_bwd(const flce_params_t* p, void* base, BwdWs* w, bool kept = false) {
   const size_t N = static_cast<size_t>(p->N);
   const int64_t bv = vocab_block(p);
   const int nblk = cdiv(p->V, bv);
   Carver c(base, 0);
   w->coef = c.take<float4>(N);
   w->dl_scale = c.take<float>(2);
-  w->dL = c.take<uint16_t>(N * static_cast<size_t>(bv));
+  w->dL = kept ? nullptr : c.take<uint16_t>(N * static_cast<size_t>(bv));
   w->dx_acc = nblk > 1 ? c.take<float>(N * static_cast<size_t>(p->H)) : nullptr;
   w->db_part = p->has_bias ? c.take<float>(static_cast<size_t>(cdiv(p->N, kBM)) * 4 * bv) : nullptr;
   return c.used() + kAlign;
@@ -258,6 +260,28 @@ size_t carve_saved(const flce_params_t* p, void* base, Saved* sv) {
   sv->ld_p = static_cast<int>(NT * kBN);
   sv->probs = c.take<__half>(N * NT * kBN);
   sv->part_m = c.take<float>(NT * N);
+  return c.used() + kAlign;
+}
+
+// State kept between flce_forward_keep and flce_backward_keep: the first
+// backward vocabulary block's q [N, ld] (ld = BVc; the block's dL staging
+// buffer, converted in place) as fp16, then the running maxima of its
+// 32-column chunks [ceil(cols / 32), N] fp32.
+struct Kept {
+  uint16_t* dq;
+  float* kmax;
+  int64_t ld;
+  int cols;
+};
+
+size_t carve_kept(const flce_params_t* p, void* base, Kept* k) {
+  const size_t N = static_cast<size_t>(p->N);
+  const int64_t bv = vocab_block(p);
+  Carver c(base, 0);
+  k->ld = bv;
+  k->cols = static_cast<int>(bv < p->V ? bv : p->V);
+  k->dq = c.take<uint16_t>(N * static_cast<size_t>(bv));
+  k->kmax = c.take<float>(static_cast<size_t>(cdiv(k->cols, 32)) * N);
   return c.used() + kAlign;
 }
 
@@ -322,17 +346,21 @@ struct Tracer {
 
 }  // namespace
 
+// saved: the full stored-probability state; kept: the kept block. At most
+// one of them is given.
 static flce_status_t forward_impl(const flce_params_t* p, const void* x, const void* W,
                                   const void* b, const int64_t* y, float* loss, float* lse,
                                   void* saved, size_t saved_bytes, void* workspace,
                                   size_t workspace_bytes, int32_t* dev_err, void* stream,
-                                  flce_trace_t* trace, float* shard_stats = nullptr);
+                                  flce_trace_t* trace, float* shard_stats = nullptr,
+                                  void* kept = nullptr, size_t kept_bytes = 0);
 static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, const float* lse,
                                    const void* saved, size_t saved_bytes, const void* x,
                                    const void* W, const void* b, const int64_t* y, void* dx,
                                    void* dW, void* db, void* workspace, size_t workspace_bytes,
                                    int32_t* dev_err, void* stream, flce_trace_t* trace,
-                                   bool shard = false);
+                                   bool shard = false, void* kept = nullptr,
+                                   size_t kept_bytes = 0);
 
 extern "C" {
 
@@ -361,9 +389,9 @@ size_t flce_workspace_size(const flce_params_t* p, int which) {
     FwdWs w;
     return carve_fwd(p, nullptr, &w);
   }
-  if (which == 1) {
+  if (which == 1 || which == 2) {
     BwdWs w;
-    return carve_bwd(p, nullptr, &w);
+    return carve_bwd(p, nullptr, &w, which == 2);
   }
   return 0;
 }
@@ -399,15 +427,33 @@ size_t flce_saved_size(const flce_params_t* p) {
   return carve_saved(p, nullptr, &sv);
 }
 
+size_t flce_kept_size(const flce_params_t* p) {
+  if (check_params(p) != FLCE_OK || p->N == 0 || !whole_vocab(p)) return 0;
+  Kept k{};
+  return carve_kept(p, nullptr, &k);
+}
+
+flce_status_t flce_forward_keep(const flce_params_t* p, const void* x, const void* W,
+                                const void* b, const int64_t* y, float* loss, float* lse,
+                                void* kept, size_t kept_bytes, void* workspace,
+                                size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                flce_trace_t* trace) {
+  if (!kept && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return forward_impl(p, x, W, b, y, loss, lse, nullptr, 0, workspace, workspace_bytes, dev_err,
+                      stream, trace, nullptr, kept, kept_bytes);
+}
+
 }  // extern "C"
 
 static flce_status_t forward_impl(const flce_params_t* p, const void* x, const void* W,
                                   const void* b, const int64_t* y, float* loss, float* lse,
                                   void* saved, size_t saved_bytes, void* workspace,
                                   size_t workspace_bytes, int32_t* dev_err, void* stream,
-                                  flce_trace_t* trace, float* shard_stats) {
+                                  flce_trace_t* trace, float* shard_stats, void* kept,
+                                  size_t kept_bytes) {
   NvtxRange nvtx_range(shard_stats ? "flce_forward_shard"
                        : saved     ? "flce_forward_store"
+                       : kept      ? "flce_forward_keep"
                                    : "flce_forward");
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
@@ -435,9 +481,16 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
     if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
   }
+  Kept kp{};  // filled by carve_kept when `kept` is given
+  if (kept) {
+    if (saved || shard_stats) return FLCE_ERR_INVALID_ARG;
+    if (kept_bytes < carve_kept(p, nullptr, &kp)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(kept)) return FLCE_ERR_ALIGNMENT;
+  }
   int sms = 0;
   if ((st = device_info(&sms)) != FLCE_OK) return st;
   carve_fwd(p, workspace, &w);
+  if (kept) carve_kept(p, kept, &kp);
   if (saved) {
     carve_saved(p, saved, &sv);
     w.part_m = sv.part_m;  // the tile maxima are part of the saved state
@@ -469,6 +522,15 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   ea.part_d = w.part_d;
   ea.part_s = w.part_s;
   ea.zy = w.zy;
+  ea.keep_cols = 0;
+  ea.keep_max = nullptr;
+  std::memset(&ea.keep_map, 0, sizeof(ea.keep_map));
+  if (kept) {
+    ea.keep_cols = kp.cols;
+    ea.keep_max = kp.kmax;
+    if (!encode_store_2d(&ea.keep_map, kp.dq, kp.cols, N, static_cast<uint64_t>(kp.ld) * 2, false))
+      return FLCE_ERR_CUDA;
+  }
   cudaError_t le;
   if (saved) {
     FwdStoreArgs sa;
@@ -479,7 +541,7 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
                           reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
   } else {
     le = launch_fwd_lse(kind, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
-                        reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
+                        kept != nullptr, reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
   }
   if (le != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_LSE)) return FLCE_ERR_CUDA;
 
@@ -550,6 +612,17 @@ extern "C" flce_status_t flce_backward_traced(const flce_params_t* p, const floa
                        workspace_bytes, dev_err, stream, trace);
 }
 
+extern "C" flce_status_t flce_backward_keep(const flce_params_t* p, const float* dloss,
+                                            const float* lse, void* kept, size_t kept_bytes,
+                                            const void* x, const void* W, const void* b,
+                                            const int64_t* y, void* dx, void* dW, void* db,
+                                            void* workspace, size_t workspace_bytes,
+                                            int32_t* dev_err, void* stream, flce_trace_t* trace) {
+  if (!kept && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return backward_impl(p, dloss, lse, nullptr, 0, x, W, b, y, dx, dW, db, workspace,
+                       workspace_bytes, dev_err, stream, trace, false, kept, kept_bytes);
+}
+
 extern "C" flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss,
                                              const float* lse, const void* saved,
                                              size_t saved_bytes, const void* x, const void* W,
@@ -567,9 +640,10 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
                                    const void* W, const void* b, const int64_t* y, void* dx,
                                    void* dW, void* db, void* workspace, size_t workspace_bytes,
                                    int32_t* dev_err, void* stream, flce_trace_t* trace,
-                                   bool shard) {
+                                   bool shard, void* kept, size_t kept_bytes) {
   NvtxRange nvtx_range(shard   ? "flce_backward_shard"
                        : saved ? "flce_backward_store"
+                       : kept  ? "flce_backward_keep"
                                : "flce_backward");
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
@@ -590,7 +664,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
       !aligned16(dW))
     return FLCE_ERR_ALIGNMENT;
   BwdWs w;
-  const size_t need = carve_bwd(p, nullptr, &w);
+  const size_t need = carve_bwd(p, nullptr, &w, kept != nullptr);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   Saved sv{};  // filled by carve_saved when `saved` is given
   if (saved) {
@@ -598,9 +672,18 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
     carve_saved(p, const_cast<void*>(saved), &sv);
   }
+  Kept kp{};  // filled by carve_kept when `kept` is given
+  if (kept) {
+    if (saved || shard) return FLCE_ERR_INVALID_ARG;
+    if (kept_bytes < carve_kept(p, nullptr, &kp)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+    if (!aligned16(kept)) return FLCE_ERR_ALIGNMENT;
+    carve_kept(p, kept, &kp);
+  }
   int sms = 0;
   if ((st = device_info(&sms)) != FLCE_OK) return st;
-  carve_bwd(p, workspace, &w);
+  carve_bwd(p, workspace, &w, kept != nullptr);
+  // The kept buffer is every block's dL staging buffer (same [N, BVc] layout).
+  if (kept) w.dL = kp.dq;
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   const int64_t bv = vocab_block(p);
@@ -645,14 +728,38 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
         !encode_2d(&mdl_mn, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, 64, kBK, f16))
       return FLCE_ERR_CUDA;
 
-    // Recompute the block's logits (or read the stored probabilities) and
-    // form dL (bf16) and db partials.
+    // Recompute the block's logits (or read the stored or kept
+    // probabilities) and form dL (bf16) and db partials.
     int db_parts = 0;
-    if (saved) {
+    const bool from_kept = kept && blk == 0;
+    if (from_kept) {
+      // In place: the kept q of block 0 becomes its dL.
+      ConvertArgs ca;
+      ca.probs = reinterpret_cast<const __half*>(kp.dq);
+      ca.ld_p = static_cast<int>(kp.ld);
+      ca.part_m = kp.kmax;
+      ca.chunk_max = 1;
+      ca.coef = w.coef;
+      ca.y = y;
+      ca.y_off = p->vocab_start;
+      ca.N = N;
+      ca.v0 = 0;
+      ca.Vb = Vb;
+      ca.dL = w.dL;
+      ca.ld_dL = static_cast<int>(bv);
+      ca.fp16 = p->input_fp16;
+      ca.dl_scale = w.dl_scale;
+      ca.db_part = w.db_part;
+      ca.ld_db = static_cast<int>(bv);
+      if (launch_convert(ca, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_CONVERT))
+        return FLCE_ERR_CUDA;
+      db_parts = convert_db_parts(N);
+    } else if (saved) {
       ConvertArgs ca;
       ca.probs = sv.probs;
       ca.ld_p = sv.ld_p;
       ca.part_m = sv.part_m;
+      ca.chunk_max = 0;
       ca.coef = w.coef;
       ca.y = y;
       ca.y_off = p->vocab_start;
@@ -665,7 +772,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
       ca.dl_scale = w.dl_scale;
       ca.db_part = w.db_part;
       ca.ld_db = static_cast<int>(bv);
-      if (launch_convert(ca, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_DLOGITS))
+      if (launch_convert(ca, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_CONVERT))
         return FLCE_ERR_CUDA;
       db_parts = convert_db_parts(N);
     }
@@ -688,7 +795,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     da.ld_db = static_cast<int>(bv);
     if (!encode_store_2d(&da.dl_map, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, false))
       return FLCE_ERR_CUDA;
-    if (!saved) {
+    if (!saved && !from_kept) {
       if (launch_dlogits(gemm_for(kind, N, Vb, H), mx_k, mw_k, g1, da, p->has_bias != 0, derr,
                          grid_for(g1, sms),
                          s) != cudaSuccess ||

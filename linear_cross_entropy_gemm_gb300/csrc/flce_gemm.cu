@@ -116,14 +116,25 @@ static cudaError_t launch_any(GemmKind kind, const CUtensorMap& a, const CUtenso
   }
 }
 
+template <bool KEEP>
+static cudaError_t launch_fwd_lse_t(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
+                                    const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
+                                    bool has_smooth, int* dev_err, int grid, cudaStream_t st) {
+  if (has_bias)
+    return has_smooth
+               ? launch_any<FwdLseEpi<true, true, KEEP>>(kind, a, b, g, ea, dev_err, grid, st)
+               : launch_any<FwdLseEpi<true, false, KEEP>>(kind, a, b, g, ea, dev_err, grid, st);
+  return has_smooth
+             ? launch_any<FwdLseEpi<false, true, KEEP>>(kind, a, b, g, ea, dev_err, grid, st)
+             : launch_any<FwdLseEpi<false, false, KEEP>>(kind, a, b, g, ea, dev_err, grid, st);
+}
+
 cudaError_t launch_fwd_lse(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
-                           bool has_smooth, int* dev_err, int grid, cudaStream_t st) {
-  if (has_bias)
-    return has_smooth ? launch_any<FwdLseEpi<true, true>>(kind, a, b, g, ea, dev_err, grid, st)
-                      : launch_any<FwdLseEpi<true, false>>(kind, a, b, g, ea, dev_err, grid, st);
-  return has_smooth ? launch_any<FwdLseEpi<false, true>>(kind, a, b, g, ea, dev_err, grid, st)
-                    : launch_any<FwdLseEpi<false, false>>(kind, a, b, g, ea, dev_err, grid, st);
+                           bool has_smooth, bool keep, int* dev_err, int grid, cudaStream_t st) {
+  return keep ? launch_fwd_lse_t<true>(kind, a, b, g, ea, has_bias, has_smooth, dev_err, grid, st)
+              : launch_fwd_lse_t<false>(kind, a, b, g, ea, has_bias, has_smooth, dev_err, grid,
+                                        st);
 }
 
 cudaError_t launch_fwd_store(GemmKind form, const CUtensorMap& a, const CUtensorMap& b,

@@ -23,9 +23,10 @@ struct DxArgs;
 // is the smaller).
 // kGemmAuto is resolved per GEMM on the host before any launch.
 enum GemmKind : int { kGemmSingle = 0, kGemmPair = 1, kGemmWide = 2, kGemmAuto = 3 };
+// keep: the kept-block forward (FwdLseArgs.keep_*).
 cudaError_t launch_fwd_lse(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const FwdLseArgs& ea, bool has_bias,
-                           bool has_smooth, int* dev_err, int grid, cudaStream_t st);
+                           bool has_smooth, bool keep, int* dev_err, int grid, cudaStream_t st);
 cudaError_t launch_dlogits(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const DlogitsArgs& ea, bool has_bias, int* dev_err,
                            int grid, cudaStream_t st);
@@ -71,12 +72,16 @@ struct PrepArgs {
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 
-// Stored-probability backward: fp16 q [N, ld_p] and tile maxima part_m
-// [tiles_v, N] -> bf16 dL block [N, ld_dL] and db partials [ceil(N/32), ld_db].
+// Stored-probability backward: fp16 q [N, ld_p] and its maxima -> bf16 dL
+// block [N, ld_dL] and db partials [ceil(N/32), ld_db]. The maxima are per
+// 256-column tile (part_m [tiles_v, N], chunk_max = 0) or per 32-column chunk
+// of the block (part_m [ceil(Vb/32), N], chunk_max = 1; then probs may be dL:
+// the kept block converts in place).
 struct ConvertArgs {
   const __half* probs;
   int ld_p;
   const float* part_m;
+  int chunk_max;
   const float4* coef;
   const int64_t* y;
   int64_t y_off;

@@ -248,17 +248,26 @@ cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, 
   return cudaGetLastError();
 }
 
-// Stored-probability backward: dL[n, v] = a_n q[n, v] 2^(m_t(n) - lse2_n)
+// Stored-probability backward: dL[n, v] = a_n q[n, v] 2^(m(n, v) - lse2_n)
 //   - c_n - t_n [v == y_n] for the vocab block [v0, v0 + Vb), q being the
-// forward's fp16 2^(z log2e - m_t). One CTA covers 32 tokens x one 256-column
-// vocab tile (one m_t per token). Thread i owns 8 columns (16-byte loads and
-// stores) of rows i/32, i/32 + 4, ..., so eight independent loads are in
-// flight per thread; the fp32 column sums over the 32 tokens (db partials,
-// row blockIdx.y) are combined through shared memory.
+// forward's fp16 2^(z log2e - m). One CTA covers 32 tokens x one 256-column
+// vocab tile. Thread i owns 8 columns (16-byte loads and stores) of rows
+// i/32, i/32 + 4, ..., so eight independent loads are in flight per thread;
+// the fp32 column sums over the 32 tokens (db partials, row blockIdx.y) are
+// combined through shared memory.
+//   kChunkMax = false: m is the maximum of the row's 256-column tile
+//     (part_m [tiles_v, N]; flce_forward_store's full saved state);
+//   kChunkMax = true: m is the running maximum of the row's 32-column chunk
+//     (part_m [ceil(Vb / 32), N]; the kept block of flce_forward_keep, which
+//     is converted in place: probs and dL are the same buffer, so q is read
+//     with plain loads).
 constexpr int kConvRows = 32;
 constexpr int kConvRowGroups = 4;  // 128 threads = 32 column groups x 4 row groups
+template <bool kChunkMax>
 __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs a) {
-  __shared__ float s_scale[kConvRows], s_c[kConvRows], s_t[kConvRows];
+  // Per row: the factor a 2^(m - lse2) for the tile (kChunkMax: per chunk).
+  __shared__ float s_scale[kChunkMax ? 8 : 1][kConvRows];
+  __shared__ float s_c[kConvRows], s_t[kConvRows];
   __shared__ int s_ty[kConvRows];
   __shared__ float s_sum[kConvRowGroups][256];
   const int tile = blockIdx.x;  // 256-column tile inside the block
@@ -268,22 +277,42 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
   const int colb = tile * 256 + cg * 8;  // block-relative first column of this thread
   if (threadIdx.x < kConvRows) {
     const int r = r0 + threadIdx.x;
-    float sc = 0.f, c = 0.f, t = 0.f;
+    float c = 0.f, t = 0.f;
     int ty = -1;
     if (r < a.N) {
       const float4 cf = a.coef[r];
-      const float mt = a.part_m[static_cast<size_t>(a.v0 / 256 + tile) * a.N + r];
-      sc = cf.y * exp2f(mt - cf.x);
       c = cf.z;
       t = cf.w;
+      if constexpr (!kChunkMax) {
+        const float mt = a.part_m[static_cast<size_t>(a.v0 / 256 + tile) * a.N + r];
+        s_scale[0][threadIdx.x] = cf.y * exp2f(mt - cf.x);
+      }
       const int64_t yv = a.y[r] - a.y_off;
       const int64_t lo = static_cast<int64_t>(a.v0) + tile * 256;
       if (yv >= lo && yv < lo + 256) ty = static_cast<int>(yv - a.v0);
+    } else if constexpr (!kChunkMax) {
+      s_scale[0][threadIdx.x] = 0.f;
     }
-    s_scale[threadIdx.x] = sc;
     s_c[threadIdx.x] = c;
     s_t[threadIdx.x] = t;
     s_ty[threadIdx.x] = ty;
+  }
+  if constexpr (kChunkMax) {
+    // 8 chunks x 32 rows of maxima, two per thread (each chunk's 32 rows are
+    // one coalesced 128-byte load).
+    const int nchunks = (a.Vb + 31) / 32;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int i = threadIdx.x + 128 * k;
+      const int ch = i >> 5, rr = i & 31;
+      const int r = r0 + rr, cidx = tile * 8 + ch;
+      float sc = 0.f;
+      if (r < a.N && cidx < nchunks) {
+        const float4 cf = a.coef[r];
+        sc = cf.y * exp2f(a.part_m[static_cast<size_t>(cidx) * a.N + r] - cf.x);
+      }
+      s_scale[ch][rr] = sc;
+    }
   }
   __syncthreads();
   const float dls = a.dl_scale[0];
@@ -295,15 +324,18 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
 #pragma unroll
   for (int k = 0; k < kConvRows / kConvRowGroups; ++k) {
     const int i = rg + kConvRowGroups * k;
-    if (r0 + i < a.N)
-      q[k] = __ldg(reinterpret_cast<const uint4*>(
-          a.probs + static_cast<size_t>(r0 + i) * a.ld_p + a.v0 + colb));
+    if (r0 + i < a.N && colb < a.Vb) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.probs + static_cast<size_t>(r0 + i) * a.ld_p + a.v0 + colb);
+      q[k] = kChunkMax ? *src : __ldg(src);
+    }
   }
 #pragma unroll
   for (int k = 0; k < kConvRows / kConvRowGroups; ++k) {
     const int i = rg + kConvRowGroups * k;
-    if (r0 + i >= a.N) continue;
+    if (r0 + i >= a.N || colb >= a.Vb) continue;
     const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
+    const float scale = s_scale[kChunkMax ? cg >> 2 : 0][i];
     float d[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -313,7 +345,7 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
     }
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      float v = fmaf(s_scale[i], d[j], -s_c[i]) - (colb + j == s_ty[i] ? s_t[i] : 0.f);
+      float v = fmaf(scale, d[j], -s_c[i]) - (colb + j == s_ty[i] ? s_t[i] : 0.f);
       v = colb + j < a.Vb ? v : 0.f;
       sum[j] += v;
       d[j] = v * dls;
@@ -340,7 +372,10 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
 
 cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st) {
   dim3 grid((a.Vb + 255) / 256, (a.N + kConvRows - 1) / kConvRows);
-  probs_to_dlogits_kernel<<<grid, 128, 0, st>>>(a);
+  if (a.chunk_max)
+    probs_to_dlogits_kernel<true><<<grid, 128, 0, st>>>(a);
+  else
+    probs_to_dlogits_kernel<false><<<grid, 128, 0, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -12,6 +12,9 @@ import torch
 
 from linear_cross_entropy_gemm_gb300 import inputs as I
 
+# Backward modes of the library (DeviceProblem.run).
+MODE_NAMES = ("recompute", "stored", "kept")
+
 LOSS_RTOL = 1e-3
 GRAD_FROB = 5e-3
 GRAD_MAX = 2.0 ** -7
@@ -40,22 +43,32 @@ class DeviceProblem:
         self.dloss = torch.from_numpy(inp.dloss).to(self.dev)
 
     def run(self, *, dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0,
-            store=False, **over):
-        """Forward + backward through the C ABI. store=True uses the
-        stored-probability mode (no logits recompute in the backward)."""
+            mode="recompute", **over):
+        """Forward + backward through the C ABI in one of the backward modes:
+        "recompute" (every vocabulary block's logits recomputed), "stored"
+        (every logit's probability kept by the forward, no recompute) or
+        "kept" (the first vocabulary block's probabilities kept, the others
+        recomputed)."""
         import linear_cross_entropy_gemm_gb300 as F
+        assert mode in MODE_NAMES, mode
         opts = opts_of(self.inp.wl)
         opts.update(over)
         wl = self.inp.wl
-        saved = None
-        if store:
+        saved = kept = None
+        if mode == "stored":
             n = F.flce_saved_size(wl.N, wl.H, wl.V, label_smoothing=opts["label_smoothing"],
                                   input_fp16=wl.dtype == "fp16")
             saved = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
-        loss, lse = F.flce_forward(self.x, self.W, self.b, self.y, saved=saved, **opts)
+        elif mode == "kept" and wl.N > 0:
+            n = F.flce_kept_size(wl.N, wl.H, wl.V, input_fp16=wl.dtype == "fp16",
+                                 bwd_vocab_block=bwd_vocab_block)
+            kept = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
+        loss, lse = F.flce_forward(self.x, self.W, self.b, self.y, saved=saved, kept=kept,
+                                   bwd_vocab_block=bwd_vocab_block, **opts)
         dx, dW, db = F.flce_backward(self.dloss, lse, self.x, self.W, self.b, self.y,
                                      dW_dtype=dW_dtype, db_dtype=db_dtype,
-                                     bwd_vocab_block=bwd_vocab_block, saved=saved, **opts)
+                                     bwd_vocab_block=bwd_vocab_block, saved=saved, kept=kept,
+                                     **opts)
         torch.cuda.synchronize(self.dev)
         err = F.flce_read_device_error(self.dev)
         return dict(loss=loss, lse=lse, dx=dx, dW=dW, db=db, err=err)

@@ -33,12 +33,12 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("store", [False, True], ids=["recompute", "stored"])
+@pytest.mark.parametrize("mode", ["recompute", "stored", "kept"])
 @pytest.mark.parametrize("case", sorted(CASES))
 @pytest.mark.parametrize("form", FORMS)
-def test_each_gemm_form_matches_the_oracle(form, case, store):
+def test_each_gemm_form_matches_the_oracle(form, case, mode):
     wl, kw = CASES[case]
-    full_check(wl, store=store, gemm_form=form, **kw)
+    full_check(wl, mode=mode, gemm_form=form, **kw)
 
 
 @pytest.mark.parametrize("warps", ["16", "8"])

@@ -1,6 +1,6 @@
 """Seeded randomized parity sweep: small random shapes (N, H, V off the tile
 grid, including single rows / columns), random loss options, bias, operand
-type, backward mode and vocabulary block, each compared element by element
+type, backward mode (recompute, stored or kept block) and vocabulary block, each compared element by element
 with the CPU oracle. The GEMM form cycles through default / single / pair /
 wide by case index (the random draws do not depend on it). The case list is
 fixed by the seed, so failures reproduce."""
@@ -40,13 +40,16 @@ def _cases(n=24, seed=20261202):
             wl = wl.with_(dloss_scale=1024.0)
         bvb = int(r.choice([0, 256, 512, 1024]))
         store = bool(r.random() < 0.4)
+        # Cases that do not store every probability alternate between the
+        # recompute and kept-block modes by index (no extra random draw).
+        mode = "stored" if store else ("kept" if i % 2 else "recompute")
         form = ("default", "single", "pair", "wide")[i % 4]
-        out.append(pytest.param(wl, bvb, store, form,
+        out.append(pytest.param(wl, bvb, mode, form,
                                 id=f"{wl.name}-N{wl.N}-H{wl.H}-V{wl.V}-{wl.dtype}"
-                                f"-{red}-bv{bvb}-{'st' if store else 'rc'}-{form}"))
+                                f"-{red}-bv{bvb}-{mode}-{form}"))
     return out
 
 
-@pytest.mark.parametrize("wl,bvb,store,form", _cases())
-def test_random_shapes_and_options(wl, bvb, store, form):
-    full_check(wl, bwd_vocab_block=bvb, store=store, gemm_form=form)
+@pytest.mark.parametrize("wl,bvb,mode,form", _cases())
+def test_random_shapes_and_options(wl, bvb, mode, form):
+    full_check(wl, bwd_vocab_block=bvb, mode=mode, gemm_form=form)

@@ -19,14 +19,14 @@ from parity import (DeviceProblem, assert_grad_close, assert_loss_close, f64, op
 pytestmark = pytest.mark.gpu
 
 
-MODES = [pytest.param(False, id="recompute"), pytest.param(True, id="stored")]
+MODES = ["recompute", "stored", "kept"]
 
 
 def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.float32,
-               store=False, gemm_form="default"):
+               mode="recompute", gemm_form="default"):
     inp = I.make_inputs(wl)
     out = DeviceProblem(inp).run(bwd_vocab_block=bwd_vocab_block, dW_dtype=dW_dtype,
-                                 db_dtype=db_dtype, store=store, gemm_form=gemm_form)
+                                 db_dtype=db_dtype, mode=mode, gemm_form=gemm_form)
     assert out["err"] == 0, f"device error word {out['err']}"
     x64, W64, b64 = f64(inp)
     opts = opts_of(wl)
@@ -41,90 +41,90 @@ def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.
     return out
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_tiny_full(store):
-    full_check(I.WORKLOADS["tiny"], store=store)
+@pytest.mark.parametrize("mode", MODES)
+def test_tiny_full(mode):
+    full_check(I.WORKLOADS["tiny"], mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_medium_full_with_bias_smoothing_zloss(store):
-    full_check(I.WORKLOADS["medium"], store=store)
+@pytest.mark.parametrize("mode", MODES)
+def test_medium_full_with_bias_smoothing_zloss(mode):
+    full_check(I.WORKLOADS["medium"], mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-def test_ragged_tails_multi_block(reduction, store):
+def test_ragged_tails_multi_block(reduction, mode):
     # N, H, V not multiples of the 128 x 256 x 64 tile; vocab blocks of 256
     # leave a 1-column last block.
     wl = I.Workload("ragged", N=129, H=72, V=257, seed=21, b_std=0.5, ignore_frac=0.1,
                     label_smoothing=0.2, lse_square_scale=1e-2, logit_scale=1.3,
                     reduction=reduction,
                     dloss="normal_per_token" if reduction == "none" else "normal_scalar")
-    full_check(wl, bwd_vocab_block=256, store=store)
+    full_check(wl, bwd_vocab_block=256, mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_degenerate_single_class_single_token(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_degenerate_single_class_single_token(mode):
     wl = I.Workload("v1", N=1, H=8, V=1, seed=22, b_std=1.0, label_smoothing=0.3,
                     lse_square_scale=0.1, reduction="sum")
-    full_check(wl, store=store)
+    full_check(wl, mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_few_tokens_many_vocab_blocks(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_few_tokens_many_vocab_blocks(mode):
     wl = I.Workload("wide", N=5, H=64, V=5000, seed=23, x_std=2.0, w_std=0.1,
                     label_smoothing=0.05, reduction="mean")
-    full_check(wl, bwd_vocab_block=1024, store=store)
+    full_check(wl, bwd_vocab_block=1024, mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_bf16_gradients_and_custom_ignore_index(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_bf16_gradients_and_custom_ignore_index(mode):
     wl = I.Workload("bf16out", N=200, H=128, V=777, seed=24, b_std=0.1, ignore_frac=0.2,
                     ignore_index=5, reduction="mean")
     full_check(wl, dW_dtype=torch.bfloat16, db_dtype=torch.bfloat16, bwd_vocab_block=512,
-               store=store)
+               mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_negative_logit_scale_and_class_zero_ignored(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_negative_logit_scale_and_class_zero_ignored(mode):
     wl = I.Workload("negscale", N=257, H=136, V=999, seed=33, b_std=0.2, ignore_frac=0.0,
                     ignore_index=0, logit_scale=-0.75, label_smoothing=0.05,
                     lse_square_scale=2e-3, reduction="mean")
-    full_check(wl, bwd_vocab_block=512, store=store)
+    full_check(wl, bwd_vocab_block=512, mode=mode)
 
 
-def test_large_logits_small_shape_both_modes():
+def test_large_logits_small_shape_every_mode():
     # logit std ~45 (x, W, b ~ N(0, 1)): most tile probabilities underflow fp16
-    # in the stored mode; the ones that matter must survive.
+    # in the stored and kept modes; the ones that matter must survive.
     wl = I.WORKLOADS["large_logit"].with_(N=300, V=3000, H=2048)
-    full_check(wl, bwd_vocab_block=1024, store=False)
-    full_check(wl, bwd_vocab_block=1024, store=True)
+    for mode in MODES:
+        full_check(wl, bwd_vocab_block=1024, mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_fp16_operands(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_fp16_operands(mode):
     wl = I.WORKLOADS["medium"].with_(name="medium_fp16", dtype="fp16", N=1000, V=5000)
-    full_check(wl, bwd_vocab_block=2048, store=store,
+    full_check(wl, bwd_vocab_block=2048, mode=mode,
                dW_dtype=torch.float16, db_dtype=torch.float16)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_fp16_loss_scaled_gradients_do_not_overflow(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_fp16_loss_scaled_gradients_do_not_overflow(mode):
     # sum reduction with a 65536 loss scale: the target column's dlogit is
     # about -65536, beyond fp16's largest finite value, before the library's
     # power-of-two dL scaling; dx itself (~3e3) and dW (fp32) stay in range.
     wl = I.Workload("fp16_scaled", N=400, H=256, V=3000, seed=28, dtype="fp16", x_std=2.0,
                     w_std=0.05, reduction="sum", dloss_scale=65536.0)
-    full_check(wl, bwd_vocab_block=1024, store=store)
+    full_check(wl, bwd_vocab_block=1024, mode=mode)
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_fp16_small_gradients_do_not_flush(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_fp16_small_gradients_do_not_flush(mode):
     # mean over 4096 tokens of a 30000-way softmax: dlogits ~ 1e-9, below fp16's
     # smallest subnormal without the library's power-of-two dL scaling.
     wl = I.Workload("fp16_tiny_grads", N=4096, H=128, V=30000, seed=29, dtype="fp16",
                     reduction="mean")
-    full_check(wl, store=store)
+    full_check(wl, mode=mode)
 
 
 def test_fp16_product_beyond_fp16_range_before_bias():
@@ -185,28 +185,29 @@ def test_out_of_range_target_sets_device_error():
     assert F.flce_read_device_error() == 0, "error word not cleared"
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_run_to_run_bitwise_determinism(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_run_to_run_bitwise_determinism(mode):
     wl = I.WORKLOADS["medium"].with_(N=1000, V=3000)
     p = DeviceProblem(I.make_inputs(wl))
-    a = p.run(bwd_vocab_block=1024, store=store)
-    b = p.run(bwd_vocab_block=1024, store=store)
+    a = p.run(bwd_vocab_block=1024, mode=mode)
+    b = p.run(bwd_vocab_block=1024, mode=mode)
     for k in ("loss", "lse", "dx", "dW", "db"):
         assert torch.equal(a[k], b[k]), f"{k} differs between runs"
 
 
-@pytest.mark.parametrize("store", MODES)
-def test_autograd_module_matches_c_abi(store):
+@pytest.mark.parametrize("mode", MODES)
+def test_autograd_module_matches_c_abi(mode):
     wl = I.Workload("module", N=256, H=128, V=1000, seed=27, b_std=0.05, ignore_frac=0.05,
                     label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.9)
     inp = I.make_inputs(wl)
     p = DeviceProblem(inp)
-    ref = p.run(store=store)
+    ref = p.run(mode=mode)
     x = p.x.clone().requires_grad_(True)
     W = p.W.clone().requires_grad_(True)
     b = p.b.clone().requires_grad_(True)
     mod = F.FusedLinearCrossEntropyLoss(label_smoothing=0.1, lse_square_scale=1e-3,
-                                        logit_scale=0.9, recompute=not store)
+                                        logit_scale=0.9, recompute=mode != "stored",
+                                        keep_block=mode == "kept")
     loss = mod(x.view(2, 128, 128), p.y.view(2, 128), W, b)
     loss.backward()
     torch.cuda.synchronize()
@@ -254,10 +255,10 @@ def _sampled(name):
     rdx = O.dx_rows(rows, dl, x64, W64, b64, inp.y, **opts)
     rdW, rdb = O.dW_db_rows(vrows, lse, dl, x64, W64, b64, inp.y, **opts)
     got = {}
-    for store in (False, True):
-        out = prob.run(store=store)
+    for mode in MODES:
+        out = prob.run(mode=mode)
         assert out["err"] == 0, f"device error word {out['err']}"
-        got[store] = dict(loss=to_np(out["loss"]), lse=to_np(out["lse"]),
+        got[mode] = dict(loss=to_np(out["loss"]), lse=to_np(out["lse"]),
                           dx=to_np(out["dx"][torch.from_numpy(rows).to(out["dx"].device)]),
                           dW=to_np(out["dW"][torch.from_numpy(vrows).to(out["dW"].device)]),
                           db=None if out["db"] is None else to_np(out["db"])[vrows])
@@ -268,11 +269,11 @@ def _sampled(name):
     return res
 
 
-@pytest.mark.parametrize("store", MODES)
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", ["llama3_head", "large_logit", "vocab256k"])
-def test_full_size_sampled(name, store):
+def test_full_size_sampled(name, mode):
     r = _sampled(name)
-    g, ref, wl = r["got"][store], r["ref"], r["wl"]
+    g, ref, wl = r["got"][mode], r["ref"], r["wl"]
     assert_loss_close(g["loss"], ref["loss"], f"{name} loss")
     assert_loss_close(g["lse"], ref["lse"], f"{name} lse (all tokens)")
     assert_grad_close(g["dx"], ref["dx"], f"{name} dx (sampled rows)")
@@ -304,9 +305,9 @@ def test_non_contiguous_inputs_are_rejected():
         F.flce_forward(x, W, None, y)
 
 
-@pytest.mark.parametrize("store", MODES)
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("N", [300, 129, 1])
-def test_no_writes_outside_caller_buffers(N, store):
+def test_no_writes_outside_caller_buffers(N, mode):
     # Every buffer the library writes gets a canary-filled guard region after
     # it (N = 300: an odd number of 128-row tiles, so a CTA pair's second half
     # is pure padding); the guards must be untouched after forward + backward.
@@ -327,13 +328,18 @@ def test_no_writes_outside_caller_buffers(N, store):
         assert bool((tail == 0xA5).all()), f"{what}: write past the end"
 
     nf = F.flce_workspace_size(N, wl.H, wl.V, "forward", **opts)
-    nb = F.flce_workspace_size(N, wl.H, wl.V, "backward", bwd_vocab_block=512, **opts)
+    nb = F.flce_workspace_size(N, wl.H, wl.V, "backward_keep" if mode == "kept" else "backward",
+                               bwd_vocab_block=512, **opts)
     wf, wb = guarded(nf), guarded(nb)
-    saved = None
-    ns = 0
-    if store:
+    state, ns, skw = None, 0, {}
+    if mode == "stored":
         ns = F.flce_saved_size(N, wl.H, wl.V, **opts)
-        saved = guarded(ns)
+        state = guarded(ns)
+        skw = dict(saved=state[:ns])
+    elif mode == "kept":
+        ns = F.flce_kept_size(N, wl.H, wl.V, bwd_vocab_block=512, **opts)
+        state = guarded(ns)
+        skw = dict(kept=state[:ns])
     lossb, lseb = guarded(4), guarded(4 * N)
     dxb, dWb, dbb = guarded(2 * N * wl.H), guarded(4 * wl.V * wl.H), guarded(4 * wl.V)
     loss = lossb[:4].view(torch.float32)
@@ -342,16 +348,16 @@ def test_no_writes_outside_caller_buffers(N, store):
     dW = dWb[:4 * wl.V * wl.H].view(torch.float32).view(wl.V, wl.H)
     db = dbb[:4 * wl.V].view(torch.float32)
     F.flce_forward(p.x, p.W, p.b, p.y, workspace=wf[:nf], out=(loss, lse),
-                   saved=None if saved is None else saved[:ns], **opts)
+                   bwd_vocab_block=512, **skw, **opts)
     F.flce_backward(p.dloss, lse, p.x, p.W, p.b, p.y, workspace=wb[:nb], out=(dx, dW, db),
-                    bwd_vocab_block=512, saved=None if saved is None else saved[:ns], **opts)
+                    bwd_vocab_block=512, **skw, **opts)
     torch.cuda.synchronize()
     assert F.flce_read_device_error(dev) == 0
     for t, n, what in ((wf, nf, "forward workspace"), (wb, nb, "backward workspace"),
                        (lossb, 4, "loss"), (lseb, 4 * N, "lse"), (dxb, 2 * N * wl.H, "dx"),
                        (dWb, 4 * wl.V * wl.H, "dW"), (dbb, 4 * wl.V, "db")):
         check(t, n, what)
-    if store:
-        check(saved, ns, "saved state")
-    ref = p.run(bwd_vocab_block=512, store=store)
+    if state is not None:
+        check(state, ns, f"{mode} state")
+    ref = p.run(bwd_vocab_block=512, mode=mode)
     assert torch.equal(ref["dW"], dW) and torch.equal(ref["db"], db)
