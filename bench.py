@@ -1,21 +1,34 @@
 """Benchmark of the fused linear cross-entropy (FLCE) forward + backward.
 
-One step = flce_forward + flce_backward (the whole hot path) over one batch
-of the Llama-3-shaped head: N=8192 tokens, H=4096, V=128256, bf16, mean
-reduction, no bias, dloss = 1. Prints ONE JSON line (rank 0).
+One step = the forward and the backward (the whole hot path) over one batch
+of a workload, by default the Llama-3-shaped head: N=8192 tokens, H=4096,
+V=128256, bf16, mean reduction, no bias, dloss = 1. Prints ONE JSON line
+(rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload tiny|medium|llama3_head|large_logit|vocab256k]
+                  [--mode kept|recompute|stored]
 
 * value: tokens/s over all ranks, inputs resident in HBM, device time per
   step from CUDA events on the launching stream; L2 flushed (256 MiB write)
   between timed steps, outside the timed events.
+* mode: the backward mode of the timed step. "kept" (the default, and the
+  autograd module's): the forward keeps the first backward vocabulary
+  block's probabilities in the buffer the backward stages dL in, and the
+  backward recomputes the other blocks. "recompute": every block recomputed.
+  "stored": every logit's probability kept (2 N V bytes more memory). The
+  two other modes are timed the same way and reported in "modes".
 * e2e: the same metric through the C ABI with the step's inputs (x, y,
   dloss) copied from pinned host memory and the loss read back every step;
-  the next step's copy runs on a side stream during the current step.
+  the next step's copy runs on a side stream during the current step. The
+  gradients stay on the device, as in a training step.
 * roofline: the dominant kernel (most device time), timed per launch with
   caller-owned CUDA events around each launch (flce_*_traced).
+* memory: peak device memory above the live inputs across one step
+  (torch's allocator; the library allocates nothing, which the device-level
+  free memory confirms), split into the library's scratch and the outputs.
 * cpu_baseline / --impl reference: the CPU fp64 oracle timed on this host's
-  cores on a bounded sample of the same workload (a slow reference
+  cores on the same bounded token sample of the workload (a slow reference
   implementation, not a target).
 * --gpus N > 1 (torchrun): independent replicas, one per GPU ("replicas
   only": the path is not sharded across GPUs); barrier + max over ranks.
@@ -31,21 +44,43 @@ import sys
 import threading
 import time
 
-import numpy as np
+
+def _oracle_threads_from_argv():
+    """--oracle-threads T fixes the BLAS thread count of the CPU oracle; it
+    must be in the environment before numpy loads its BLAS library."""
+    for i, a in enumerate(sys.argv):
+        if a == "--oracle-threads" and i + 1 < len(sys.argv):
+            return sys.argv[i + 1]
+        if a.startswith("--oracle-threads="):
+            return a.split("=", 1)[1]
+    return None
+
+
+_T = _oracle_threads_from_argv()
+if _T:
+    for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[_v] = _T
+
+import numpy as np  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "llama3_head"
 METRIC = "FLCE fwd+bwd ms, tokens/s, TFLOP/s (% bf16 TC peak) @ 8192×4096×128256"
-PAGES_MS = 19.897  # Liger-Kernel commit 95b01e9, B200, same shape (context)
+HEADLINE = "llama3_head"
+PAGES_MS = 19.897  # Liger-Kernel commit 95b01e9, B200, Llama-3 head shape (context)
 L2_FLUSH_BYTES = 256 << 20
-# dram__bytes_read.sum + dram__bytes_write.sum per launch (average over the
-# step's launches of that kernel) from one ncu capture of this workload's full
-# step (1-pass metrics; profiles/dram_traffic_llama3_head.md). Must be
-# re-measured (or removed) whenever one of these kernels or its raster changes.
-TRAFFIC_PER_LAUNCH = {"fwd_lse": 2.986e9, "bwd_dlogits": 3.138e9, "bwd_dw": 4.212e9,
-                      "bwd_dx": 5.979e9}
+MODES = ("kept", "recompute", "stored")
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, averaged over a
+# step's launches of each kernel, from one ncu capture of the Llama-3 head
+# step in the recompute mode (1-pass metrics, default GEMM forms and block,
+# the committed build of these kernels). Not measured by this run; reported
+# only for that exact configuration and labelled as such.
+TRAFFIC_CAPTURE = {"fwd_lse": 2.986e9, "bwd_dlogits": 3.138e9, "bwd_dw": 4.212e9,
+                   "bwd_dx": 5.979e9}
+TRAFFIC_SOURCE = ("ncu capture of the recompute-mode Llama-3 head step on another GB300 "
+                  "(dram__bytes_read.sum + dram__bytes_write.sum per launch); not measured "
+                  "in this run")
 
 
 def peaks():
@@ -91,7 +126,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for ln in self.lines:
             f = [t.strip() for t in ln.split(",")]
@@ -100,6 +135,7 @@ class ClockSampler:
             try:
                 sm.append(float(f[0]))
                 mx.append(float(f[1]))
+                pw.append(float(f[2]))
             except ValueError:
                 continue
             for name, val in zip(names, f[4:8]):
@@ -107,6 +143,7 @@ class ClockSampler:
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -127,6 +164,41 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
 
 
+def workload_of(args):
+    from linear_cross_entropy_gemm_gb300 import inputs as I
+    wl = I.WORKLOADS[args.workload]
+    if args.shape:
+        n_, h_, v_ = (int(t) for t in args.shape.split(","))
+        wl = wl.with_(name=f"{wl.name}-shape", N=n_, H=h_, V=v_)
+    if args.dtype != wl.dtype:
+        wl = wl.with_(dtype=args.dtype)
+    return wl
+
+
+def config_of(wl, ws: int) -> dict:
+    """The workload's description, the same in both arms' JSON lines."""
+    opts = [wl.reduction, "bias" if wl.has_bias else "no bias"]
+    if wl.label_smoothing:
+        opts.append(f"label_smoothing={wl.label_smoothing:g}")
+    if wl.lse_square_scale:
+        opts.append(f"lse_square_scale={wl.lse_square_scale:g}")
+    if wl.logit_scale != 1.0:
+        opts.append(f"logit_scale={wl.logit_scale:g}")
+    if wl.ignore_frac:
+        opts.append(f"{wl.n_ignored} ignored")
+    opts.append(f"dloss={wl.dloss}")
+    return {"workload": f"{wl.name}: N={wl.N} H={wl.H} V={wl.V} {wl.dtype}, " + ", ".join(opts),
+            "N": wl.N, "H": wl.H, "V": wl.V, "dtype": wl.dtype,
+            "parallelism": "replicas" if ws > 1 else "single GPU",
+            "l2": "GPU arm: flushed (256 MiB write) before each timed step, outside the events"}
+
+
+def options_of(wl) -> dict:
+    return dict(ignore_index=wl.ignore_index, label_smoothing=wl.label_smoothing,
+                lse_square_scale=wl.lse_square_scale, logit_scale=wl.logit_scale,
+                reduction=wl.reduction)
+
+
 # ----------------------------------------------------------- CPU oracle arm
 
 class OracleSample:
@@ -136,12 +208,10 @@ class OracleSample:
     def __init__(self, wl, rows: int):
         from linear_cross_entropy_gemm_gb300 import inputs as I
         inp = I.make_inputs(wl.with_(N=rows))
-        self.x, self.W = I.bf16_bits_to_f64(inp.x), I.bf16_bits_to_f64(inp.W)
-        self.b = None if inp.b is None else I.bf16_bits_to_f64(inp.b)
+        self.x, self.W = I.bits_to_f64(inp.x, wl.dtype), I.bits_to_f64(inp.W, wl.dtype)
+        self.b = None if inp.b is None else I.bits_to_f64(inp.b, wl.dtype)
         self.y, self.dloss = inp.y, inp.dloss.astype(np.float64)
-        self.opts = dict(ignore_index=wl.ignore_index, label_smoothing=wl.label_smoothing,
-                         lse_square_scale=wl.lse_square_scale, logit_scale=wl.logit_scale,
-                         reduction=wl.reduction)
+        self.opts = options_of(wl)
 
     def run(self) -> float:
         from oracle import flce_oracle as O
@@ -151,39 +221,52 @@ class OracleSample:
         return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, rows: int):
-    secs, cores = OracleSample(wl, rows).run(), os.cpu_count()
-    return {"value": rows / secs, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{rows} of {wl.N} tokens of {wl.name} (all V={wl.V}, H={wl.H}); "
-                      f"numpy float64 forward + backward, {secs:.1f} s"}
+def oracle_threads() -> int:
+    t = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS")
+    return int(t) if t else (os.cpu_count() or 1)
+
+
+def sample_text(wl, rows: int, reps: int, secs: float) -> str:
+    return (f"{rows} of {wl.N} tokens of {wl.name} per step (all V={wl.V}, H={wl.H}); "
+            f"numpy float64 forward + backward, {reps} steps in {secs:.1f} s")
+
+
+def cpu_baseline(wl, rows: int, min_seconds: float = 10.0):
+    """The oracle over the sample, repeated until about min_seconds of work."""
+    s = OracleSample(wl, rows)
+    times = []
+    while sum(times) < min_seconds or len(times) < 2:
+        times.append(s.run())
+    per_step = statistics.median(times)
+    return {"value": rows / per_step, "unit": "tokens/s", "cores": oracle_threads(),
+            "kind": "oracle", "sample": sample_text(wl, rows, len(times), sum(times)),
+            "ms_per_sampled_step": per_step * 1e3,
+            "extrapolated_ms_per_full_step": per_step / rows * wl.N * 1e3}
 
 
 def run_reference(args):
     rank, _, ws = dist_env()
     if rank != 0:
         return
-    from linear_cross_entropy_gemm_gb300 import inputs as I
-    wl = I.WORKLOADS[WORKLOAD]
-    if args.shape:
-        n_, h_, v_ = (int(t) for t in args.shape.split(","))
-        wl = wl.with_(name=f"{wl.name}-shape", N=n_, H=h_, V=v_)
-    rows = min(args.ref_rows, wl.N)
+    wl = workload_of(args)
+    rows = min(args.sample_rows, wl.N)
     sample = OracleSample(wl, rows)
     for _ in range(min(args.warmup, 1)):
         sample.run()
     times = [sample.run() for _ in range(args.steps)]
-    cores = os.cpu_count()
-    per_tok = sum(times) / (rows * len(times))
-    value = 1.0 / per_tok
+    per_step = sum(times) / len(times)
+    value = rows / per_step
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": per_tok * wl.N * 1e3, "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{wl.name} N={wl.N} H={wl.H} V={wl.V} bf16 inputs, mean",
-                   "sample_tokens_per_step": rows, "extrapolated": "ms_per_step = per-token time x N"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{rows} tokens per step of {wl.N}"},
+        "config": config_of(wl, ws),
+        "step": f"one oracle forward + backward over {rows} of the workload's {wl.N} tokens",
+        "extrapolated_ms_per_full_step": per_step / rows * wl.N * 1e3,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(),
+                         "kind": "oracle", "sample": sample_text(wl, rows, len(times),
+                                                                 sum(times))},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -192,14 +275,94 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
-def end_to_end(torch, stream, step, dev_in, host_in, loss, host_loss, steps, barrier):
+class Problem:
+    """Device inputs of one workload plus the buffers of one backward mode,
+    and one forward + backward step through the binding (C ABI)."""
+
+    def __init__(self, torch, F, wl, dev, tdt, fkw, bkw):
+        from linear_cross_entropy_gemm_gb300 import inputs as I
+        self.torch, self.F, self.wl, self.dev = torch, F, wl, dev
+        self.fkw, self.bkw = fkw, bkw
+        inp = I.make_inputs(wl)
+        self.host_x = torch.from_numpy(inp.x.view(np.int16)).view(tdt).pin_memory()
+        self.host_y = torch.from_numpy(inp.y).pin_memory()
+        self.host_dl = torch.from_numpy(inp.dloss).pin_memory()
+        self.x = self.host_x.to(dev)
+        self.W = torch.from_numpy(inp.W.view(np.int16)).view(tdt).to(dev)
+        self.b = None if inp.b is None else torch.from_numpy(inp.b.view(np.int16)).view(tdt).to(dev)
+        self.y = self.host_y.to(dev)
+        self.dloss = self.host_dl.to(dev)
+        self.opts = options_of(wl)
+        self.tdt = tdt
+        self.bufs = None
+
+    def allocate(self, mode):
+        torch, F, wl = self.torch, self.F, self.wl
+        N, H, V, dev = wl.N, wl.H, wl.V, self.dev
+        bvb = self.bkw.get("bwd_vocab_block", 0)
+        fp16 = self.tdt == torch.float16
+        b = {"mode": mode}
+        b["fws"] = torch.empty(F.flce_workspace_size(N, H, V, "forward", **self.opts),
+                               dtype=torch.uint8, device=dev)
+        kind = "backward_keep" if mode == "kept" else "backward"
+        b["bws"] = torch.empty(F.flce_workspace_size(N, H, V, kind, bwd_vocab_block=bvb,
+                                                     has_bias=wl.has_bias, **self.opts),
+                               dtype=torch.uint8, device=dev)
+        b["state"] = None
+        if mode == "stored":
+            b["state"] = torch.empty(F.flce_saved_size(N, H, V, input_fp16=fp16, **self.opts),
+                                     dtype=torch.uint8, device=dev)
+        elif mode == "kept":
+            b["state"] = torch.empty(F.flce_kept_size(N, H, V, input_fp16=fp16,
+                                                      bwd_vocab_block=bvb), dtype=torch.uint8,
+                                     device=dev)
+        b["loss"] = torch.empty(N if wl.reduction == "none" else 1, dtype=torch.float32, device=dev)
+        b["lse"] = torch.empty(N, dtype=torch.float32, device=dev)
+        b["dx"] = torch.empty(N, H, dtype=self.tdt, device=dev)
+        b["dW"] = torch.empty(V, H, dtype=torch.float32, device=dev)
+        b["db"] = torch.empty(V, dtype=torch.float32, device=dev) if wl.has_bias else None
+        self.bufs = b
+        return b
+
+    def release(self):
+        self.bufs = None
+
+    def scratch_bytes(self):
+        b = self.bufs
+        return sum(t.numel() for t in (b["fws"], b["bws"], b["state"]) if t is not None)
+
+    def output_bytes(self):
+        b = self.bufs
+        return sum(t.numel() * t.element_size()
+                   for t in (b["loss"], b["lse"], b["dx"], b["dW"], b["db"]) if t is not None)
+
+    def step(self, ftr=None, btr=None, xb=None, yb=None, dlb=None):
+        F, b = self.F, self.bufs
+        xb = self.x if xb is None else xb
+        yb = self.y if yb is None else yb
+        dlb = self.dloss if dlb is None else dlb
+        st = {} if b["state"] is None else {("saved" if b["mode"] == "stored" else "kept"):
+                                            b["state"]}
+        F.flce_forward(xb, self.W, self.b, yb, workspace=b["fws"], out=(b["loss"], b["lse"]),
+                       trace=ftr, bwd_vocab_block=self.bkw.get("bwd_vocab_block", 0),
+                       **st, **self.opts, **self.fkw)
+        F.flce_backward(dlb, b["lse"], xb, self.W, self.b, yb, workspace=b["bws"],
+                        out=(b["dx"], b["dW"], b["db"]), trace=btr, **st, **self.opts,
+                        **self.bkw)
+
+
+def end_to_end(torch, stream, prob, steps, barrier):
     """Milliseconds per step of `steps` steps, each fed from the host: copy the
-    step's inputs (host_in, pinned) into one of two device buffer sets on a
-    copy stream, run step(xb, yb, dlb) on `stream` once they have landed, and
-    read the loss back. The copy of step i+1 waits only for step i-1 (the last
-    user of its buffer set)."""
-    dev = dev_in[0].device
-    bufs = [dev_in, tuple(torch.empty_like(t) for t in dev_in)]
+    step's inputs (pinned x, y, dloss) into one of two device buffer sets on a
+    copy stream, run the step on `stream` once they have landed, and read the
+    loss back. The copy of step i+1 waits only for step i-1 (the last user of
+    its buffer set)."""
+    dev = prob.x.device
+    host_in = (prob.host_x, prob.host_y, prob.host_dl)
+    bufs = [(prob.x, prob.y, prob.dloss),
+            (torch.empty_like(prob.x), torch.empty_like(prob.y), torch.empty_like(prob.dloss))]
+    loss = prob.bufs["loss"]
+    host_loss = torch.empty(loss.numel(), dtype=torch.float32).pin_memory()
     copy_stream = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     free = [torch.cuda.Event(), torch.cuda.Event()]
@@ -219,7 +382,7 @@ def end_to_end(torch, stream, step, dev_in, host_in, loss, host_loss, steps, bar
                 h2d(i + 1)
             stream.wait_event(ready[i % 2])
             xb, yb, dlb = bufs[i % 2]
-            step(xb=xb, yb=yb, dlb=dlb)
+            prob.step(xb=xb, yb=yb, dlb=dlb)
             free[i % 2].record(stream)
             host_loss.copy_(loss, non_blocking=True)
 
@@ -231,7 +394,47 @@ def end_to_end(torch, stream, step, dev_in, host_in, loss, host_loss, steps, bar
     run(steps)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    return e0.elapsed_time(e1) / steps
+    h2d_bytes = sum(t.numel() * t.element_size() for t in host_in)
+    return e0.elapsed_time(e1) / steps, h2d_bytes, host_loss.numel() * 4
+
+
+def kernel_flops(name, wl, bv, mode):
+    """Algorithmic flops per step of each GEMM kernel in a backward mode."""
+    N, H, V = wl.N, wl.H, wl.V
+    kept_cols = min(bv, V) if mode == "kept" else 0
+    f = {"fwd_lse": 2.0 * N * H * V, "bwd_dw": 2.0 * N * H * V, "bwd_dx": 2.0 * N * H * V}
+    if mode != "stored":
+        f["bwd_dlogits"] = 2.0 * N * H * (V - kept_cols)
+    return f.get(name)
+
+
+def timed_steps(torch, prob, args, stream, flush, barrier, clocks=None):
+    """K device-timed steps (L2 flushed before each, outside the events) with
+    per-launch events; returns (ms per step, {kernel: [ms per launch]}, launches)."""
+    F = prob.F
+    ftr, btr = F.KernelTrace(16), F.KernelTrace(256)
+    for _ in range(args.warmup):
+        prob.step()
+    barrier()
+    if clocks:
+        clocks.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    per_kernel, launches = {}, 0
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        prob.step(ftr=ftr, btr=btr)
+        ev[i][1].record(stream)
+        torch.cuda.synchronize(prob.dev)
+        for name, ms in ftr.launches() + btr.launches():
+            per_kernel.setdefault(name, []).append(ms)
+            launches += 1
+    barrier()
+    clk = clocks.stop() if clocks else None
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    return ms, per_kernel, launches, clk
 
 
 def run_ours(args):
@@ -239,204 +442,154 @@ def run_ours(args):
     import torch.distributed as dist
 
     import linear_cross_entropy_gemm_gb300 as F
-    from linear_cross_entropy_gemm_gb300 import inputs as I
+    from linear_cross_entropy_gemm_gb300 import tuning
 
     rank, local, ws = dist_env()
     if ws > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = I.WORKLOADS[WORKLOAD]
-    if args.shape:
-        n_, h_, v_ = (int(t) for t in args.shape.split(","))
-        wl = wl.with_(name=f"{wl.name}-shape", N=n_, H=h_, V=v_)
-    if args.dtype != wl.dtype:
-        wl = wl.with_(dtype=args.dtype)
-    tdt = torch.float16 if args.dtype == "fp16" else torch.bfloat16
+    wl = workload_of(args)
+    tdt = torch.float16 if wl.dtype == "fp16" else torch.bfloat16
     pk = peaks()
-
-    inp = I.make_inputs(wl)
-    host_x = torch.from_numpy(inp.x.view(np.int16)).view(tdt).pin_memory()
-    host_y = torch.from_numpy(inp.y).pin_memory()
-    host_dl = torch.from_numpy(inp.dloss).pin_memory()
-    x = host_x.to(dev)
-    W = torch.from_numpy(inp.W.view(np.int16)).view(tdt).to(dev)
-    y = host_y.to(dev)
-    dloss = host_dl.to(dev)
-    opts = dict(ignore_index=wl.ignore_index, label_smoothing=wl.label_smoothing,
-                lse_square_scale=wl.lse_square_scale, logit_scale=wl.logit_scale,
-                reduction=wl.reduction)
     N, H, V = wl.N, wl.H, wl.V
-    from linear_cross_entropy_gemm_gb300 import tuning
-    tune = None
     fkw, bkw = {}, {"bwd_vocab_block": args.bwd_vocab_block}
+    tune = None
+    prob = Problem(torch, F, wl, dev, tdt, fkw, bkw)
     if args.autotune:
-        res = tuning.autotune(x, W, None, y, dloss=dloss, reps=3, **opts)
-        fkw, bkw = res.config.forward_kwargs(), res.config.backward_kwargs()
+        res = tuning.autotune(prob.x, prob.W, prob.b, prob.y, dloss=prob.dloss, reps=3,
+                              **prob.opts)
+        fkw.update(res.config.forward_kwargs())
+        bkw.update(res.config.backward_kwargs())
         tune = res.as_dict()
     bvb = bkw["bwd_vocab_block"]
     bv_used = bvb or tuning.library_default_block(N, V)
     forms_used = {gm: F.resolved_gemm_form(N, H, V, (fkw if gm == "fwd_lse" else bkw).get(
         "gemm_form", "default"), gemm=gm, bwd_vocab_block=bvb) for gm in F.GEMMS}
-    fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", **opts), dtype=torch.uint8, device=dev)
-    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", bwd_vocab_block=bvb,
-                                            **opts), dtype=torch.uint8, device=dev)
-    loss = torch.empty(1, dtype=torch.float32, device=dev)
-    lse = torch.empty(N, dtype=torch.float32, device=dev)
-    dx = torch.empty(N, H, dtype=tdt, device=dev)
-    dW = torch.empty(V, H, dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    ftr, btr = F.KernelTrace(8), F.KernelTrace(256)
-    host_loss = torch.empty(1, dtype=torch.float32).pin_memory()
-
-    def step(trace=False, xb=x, yb=y, dlb=dloss):
-        F.flce_forward(xb, W, None, yb, workspace=fws, out=(loss, lse),
-                       trace=ftr if trace else None, **opts, **fkw)
-        F.flce_backward(dlb, lse, xb, W, None, yb, workspace=bws, out=(dx, dW, None),
-                        trace=btr if trace else None, **opts, **bkw)
 
     def barrier():
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    for _ in range(args.warmup):
-        step()
-    barrier()
-
-    # ---- device-timed steps (inputs resident), L2 flushed between steps
-    clocks = ClockSampler(local)
-    clocks.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    per_kernel = {}
-    launches = 0
-    barrier()
-    t_wall = time.perf_counter()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        step(trace=True)
-        ev[i][1].record(stream)
-        torch.cuda.synchronize(dev)
-        for name, ms in ftr.launches() + btr.launches():
-            per_kernel.setdefault(name, []).append(ms)
-            launches += 1
-    barrier()
-    wall = time.perf_counter() - t_wall
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), ws, dev)
-
-    # ---- stored-probability backward (no logits recompute), same timing rules
-    stored = None
-    if not args.no_stored_mode:
-        saved = torch.empty(F.flce_saved_size(N, H, V, input_fp16=args.dtype == "fp16", **opts),
-                            dtype=torch.uint8, device=dev)
-
-        def step_stored(trace=False):
-            F.flce_forward(x, W, None, y, workspace=fws, out=(loss, lse), saved=saved,
-                           trace=ftr if trace else None, **opts, **fkw)
-            F.flce_backward(dloss, lse, x, W, None, y, workspace=bws, out=(dx, dW, None),
-                            saved=saved, trace=btr if trace else None, **opts, **bkw)
-
-        for _ in range(args.warmup):
-            step_stored()
+    modes = [args.mode] + ([] if args.only_mode else [m for m in MODES if m != args.mode])
+    results = {}
+    for mode in modes:
+        # Memory: everything allocated above the live inputs across one step.
         barrier()
-        sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        sk = {}
-        for i in range(args.steps):
-            flush.zero_()
-            sev[i][0].record(stream)
-            step_stored(trace=True)
-            sev[i][1].record(stream)
-            torch.cuda.synchronize(dev)
-            for name, kms in ftr.launches() + btr.launches():
-                sk.setdefault(name, []).append(kms)
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        prob.allocate(mode)
+        prob.step()
         barrier()
-        sms = max_over_ranks(sum(a.elapsed_time(b) for a, b in sev) / args.steps, ws, dev)
-        stored = {"ms_per_step": sms, "value": ws * N / (sms * 1e-3), "unit": "tokens/s",
-                  "tflops_6nhv": 6.0 * N * H * V / (sms * 1e-3) / 1e12,
-                  "saved_bytes": saved.numel(),
-                  "kernels": {("bwd_convert" if k == "bwd_dlogits" else
-                               "fwd_lse_store" if k == "fwd_lse" else k):
-                              {"launches_per_step": len(v) // args.steps,
-                               "ms_per_step": sum(v) / args.steps} for k, v in sorted(sk.items())},
-                  "note": "flce_forward_store/flce_backward_store: fp16 tile probabilities "
-                          "kept from the forward, no logits recompute (6NHV flops)"}
-        del saved
+        free0 = torch.cuda.mem_get_info(dev)[0]
+        prob.step()
+        barrier()
+        free1 = torch.cuda.mem_get_info(dev)[0]
+        mem = {"peak_extra_mib": (torch.cuda.max_memory_allocated(dev) - base) / 2**20,
+               "scratch_mib": prob.scratch_bytes() / 2**20,
+               "outputs_mib": prob.output_bytes() / 2**20,
+               "device_free_drop_during_step_mib": (free0 - free1) / 2**20}
+        clocks = ClockSampler(local) if mode == args.mode else None
+        ms, per_kernel, launches, clk = timed_steps(torch, prob, args, stream, flush, barrier,
+                                                    clocks)
+        ms = max_over_ranks(ms, ws, dev)
+        e2e = None
+        if mode == args.mode:
+            e2e = end_to_end(torch, stream, prob, args.steps, barrier)
+            e2e = (max_over_ranks(e2e[0], ws, dev), e2e[1], e2e[2])
+        results[mode] = dict(ms=ms, per_kernel=per_kernel, launches=launches, clk=clk, mem=mem,
+                             e2e=e2e)
+        prob.release()
 
-    # ---- end to end through the C ABI with host buffers. Every step's inputs
-    # are copied from pinned host memory and its loss read back inside the
-    # timed region; step i+1's copy runs on a side stream while step i
-    # computes (two device input buffers), so the copies overlap the kernels.
-    e2e_ms = end_to_end(torch, stream, step, (x, y, dloss), (host_x, host_y, host_dl), loss,
-                        host_loss, args.steps, barrier)
-    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
-
-    # ---- roofline of the dominant kernel
-    flops_per = {"fwd_lse": 2.0 * N * H * V, "bwd_dlogits": 2.0 * N * H * V,
-                 "bwd_dw": 2.0 * N * H * V, "bwd_dx": 2.0 * N * H * V}
-    totals = {k: sum(v) for k, v in per_kernel.items()}
-    dom = max(totals, key=totals.get)
+    head = results[args.mode]
+    ms, per_kernel = head["ms"], head["per_kernel"]
     steps_ = args.steps
-    dom_ms_per_step = totals[dom] / steps_
-    tensor_dom = dom in flops_per
-    if tensor_dom:
-        achieved = flops_per[dom] / (dom_ms_per_step * 1e-3) / 1e12
-        peak = pk["bf16_sus"]
-        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"bf16 sustained, {pk['src']}",
-                "launches_per_step": len(per_kernel[dom]) // steps_,
-                "ms_per_step": dom_ms_per_step,
-                "algorithmic_flops_per_step": flops_per[dom],
-                "traffic": (TRAFFIC_PER_LAUNCH.get(dom) if (N, H, V) == (8192, 4096, 128256)
-                            and args.dtype == "bf16"
-                            and bv_used == tuning.library_default_block(N, V)
-                            and forms_used == {"fwd_lse": "wide", "bwd_dlogits": "wide",
-                                               "bwd_dw": "wide", "bwd_dx": "pair"}
-                            and os.environ.get("FLCE_RASTER", "1") != "0" else None),
-                "traffic_unit": "bytes per launch (ncu dram read + write)"}
+    totals = {k: sum(v) for k, v in per_kernel.items()}
+    kern = {k: {"launches_per_step": len(v) // steps_, "ms_per_step": sum(v) / steps_,
+                "share": sum(v) / sum(totals.values())} for k, v in sorted(per_kernel.items())}
+    dom = max(totals, key=totals.get)
+    dom_ms = totals[dom] / steps_
+    dom_flops = kernel_flops(dom, wl, bv_used, args.mode)
+    if dom_flops is not None:
+        achieved = dom_flops / (dom_ms * 1e-3) / 1e12
+        default_cfg = ((N, H, V) == (8192, 4096, 128256) and wl.dtype == "bf16"
+                       and bv_used == tuning.library_default_block(N, V)
+                       and forms_used == {"fwd_lse": "wide", "bwd_dlogits": "wide",
+                                          "bwd_dw": "wide", "bwd_dx": "pair"}
+                       and os.environ.get("FLCE_RASTER", "1") != "0"
+                       and dom in ("bwd_dw", "bwd_dx"))
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": pk["bf16_sus"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_sus"],
+                "peak_kind": f"bf16 sustained ({pk['src']}); the kernel is timed inside a long step",
+                "frac_of_burst_peak": achieved / pk["bf16"],
+                "launches_per_step": len(per_kernel[dom]) // steps_, "ms_per_step": dom_ms,
+                "algorithmic_flops_per_step": dom_flops,
+                "traffic": TRAFFIC_CAPTURE[dom] if default_cfg else None,
+                "traffic_unit": "bytes per launch",
+                "traffic_source": TRAFFIC_SOURCE if default_cfg else None}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm"],
                 "unit": "GB/s", "frac": None, "traffic": None}
-    tflops = 8.0 * N * H * V / (ms * 1e-3) / 1e12
+    flops_8 = 8.0 * N * H * V
+    executed = sum(kernel_flops(k, wl, bv_used, args.mode) or 0.0 for k in totals)
+    tflops = flops_8 / (ms * 1e-3) / 1e12
     value = ws * N / (ms * 1e-3)
-    kern = {k: {"launches_per_step": len(v) // steps_, "ms_per_step": sum(v) / steps_,
-                "share": sum(v) / sum(totals.values())} for k, v in sorted(per_kernel.items())}
+    e2e_ms, h2d, d2h = head["e2e"]
+    other = {}
+    for m, r in results.items():
+        if m == args.mode:
+            continue
+        other[m] = {"ms_per_step": r["ms"], "value": ws * N / (r["ms"] * 1e-3),
+                    "unit": "tokens/s", "tflops_8nhv_equivalent": flops_8 / (r["ms"] * 1e-3) / 1e12,
+                    "memory": r["mem"],
+                    "kernels": {k: {"launches_per_step": len(v) // steps_,
+                                    "ms_per_step": sum(v) / steps_}
+                                for k, v in sorted(r["per_kernel"].items())}}
+    budget = {
+        # The library's scratch bound: one [N, BVc] 16-bit block (dL staging,
+        # or the kept probabilities) and the kept block's per-32-column maxima,
+        # the fp32 dx accumulator, the forward's per-tile partials and the
+        # per-token coefficients.
+        "scratch_bound_mib": (N * bv_used * 2 + N * (bv_used // 32) * 4 + N * H * 4
+                              + N * -(-V // 256) * 12 + N * 32) / 2**20 + 1,
+        # The same with the stated reading of "one [N, BV] tile set plus the
+        # fp32 dW accumulator": the dL block and a [V, H] fp32 dW.
+        "north_star_budget_mib": (N * bv_used * 2 + V * H * 4) / 2**20,
+    }
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": (value / (ws * N / (PAGES_MS * 1e-3)) if args.dtype == "bf16" and
+        "vs_baseline": (value / (ws * N / (PAGES_MS * 1e-3)) if wl.dtype == "bf16" and
                         (N, H, V) == (8192, 4096, 128256) else None),
-        "dtype": args.dtype, "data": "synthetic",
-        "config": {"workload": f"{wl.name}: N={N} H={H} V={V} {args.dtype}, mean, no bias, dloss=1",
-                   "parallelism": "replicas" if ws > 1 else "single GPU",
-                   "l2": "flushed (256 MiB write) before each timed step, outside the events",
-                   "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
-                   "gemm_form": forms_used,
-                   "N": N, "H": H, "V": V},
+        "dtype": wl.dtype, "data": "synthetic",
+        "config": config_of(wl, ws),
+        "impl_config": {"mode": args.mode, "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
+                        "gemm_form": forms_used},
         "tflops_8nhv": tflops, "frac_bf16_peak_8nhv": tflops / pk["bf16_sus"],
+        "frac_bf16_burst_8nhv": tflops / pk["bf16"],
+        "tflops_executed": executed / (ms * 1e-3) / 1e12,
+        "flops_executed_per_step": executed,
         "tflops_6nhv_useful": tflops * 0.75,
         "roofline": roof,
         "kernels": kern,
-        "gpu_launches": launches,
-        "e2e": {"value": ws * N / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": host_x.numel() * 2 + host_y.numel() * 8 + host_dl.numel() * 4,
-                "d2h_bytes_per_step": 4},
-        "clocks": clk,
-        "wall_s_timed": wall,
-        "stored_mode": stored,
+        "gpu_launches": head["launches"],
+        "memory": dict(head["mem"], **budget),
+        "e2e": {"value": ws * N / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "x, y, dloss copied in and the loss read back every step; dx, dW "
+                        "(and db) stay on the device, as in a training step"},
+        "clocks": head["clk"],
+        "modes": other,
     }
     if tune is not None:
         line["autotune"] = tune
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
+        line["cpu_baseline"] = cpu_baseline(wl, min(args.sample_rows, N))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -444,16 +597,22 @@ def run_ours(args):
 
 
 def main():
+    from linear_cross_entropy_gemm_gb300 import inputs as I
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=1024)
-    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(I.WORKLOADS))
+    ap.add_argument("--mode", default="kept", choices=MODES,
+                    help="backward mode of the timed step (the others are timed beside it)")
+    ap.add_argument("--only-mode", action="store_true", help="time --mode only")
+    ap.add_argument("--sample-rows", type=int, default=256,
+                    help="tokens per oracle step (reference arm and cpu_baseline)")
+    ap.add_argument("--oracle-threads", default=None,
+                    help="BLAS threads of the CPU oracle (default: all cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--shape", default="", help="N,H,V override (profiling captures only)")
-    ap.add_argument("--no-stored-mode", action="store_true")
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp16"],
                     help="operand type (the headline workload is bf16; fp16 is a side measurement)")
     ap.add_argument("--autotune", action="store_true",

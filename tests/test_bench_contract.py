@@ -22,12 +22,24 @@ def _run(args, timeout=600):
 
 def test_reference_arm_line():
     d = _run(["--impl", "reference", "--steps", "2", "--warmup", "1", "--shape", "64,128,2048",
-              "--ref-rows", "16"])
+              "--sample-rows", "16"])
     for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "cpu_baseline", "e2e", "config"):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+    # The measured time of one sampled step, not an extrapolation to the workload.
+    assert d["ms_per_step"] < 60_000 and d["extrapolated_ms_per_full_step"] >= d["ms_per_step"]
+    assert d["config"]["workload"].startswith("llama3_head")
+
+
+def test_reference_arm_other_workload_full_oracle():
+    # The tiny workload's oracle runs on all its tokens (sample = N).
+    d = _run(["--impl", "reference", "--steps", "1", "--warmup", "0", "--workload", "tiny",
+              "--sample-rows", "512", "--oracle-threads", "1"])
+    assert d["config"]["workload"].startswith("tiny") and d["config"]["N"] == 512
+    assert d["cpu_baseline"]["cores"] == 1
+    assert abs(d["extrapolated_ms_per_full_step"] - d["ms_per_step"]) < 1e-6 * d["ms_per_step"]
 
 
 @pytest.mark.gpu
@@ -35,10 +47,16 @@ def test_gpu_arm_line():
     d = _run(["--steps", "3", "--warmup", "3", "--shape", "1024,256,8192", "--no-cpu-baseline"])
     for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
               "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
-              "roofline", "e2e", "gpu_launches", "clocks", "stored_mode"):
+              "roofline", "e2e", "gpu_launches", "clocks", "modes", "memory"):
         assert k in d, k
     r = d["roofline"]
     assert r["bound"] == "tensor" and 0 < r["frac"] < 1.5 and r["unit"] == "TFLOP/s"
     assert d["gpu_launches"] == 3 * (3 + 1 + 3)  # fwd, merge, finalize; prep; one block
     assert d["e2e"]["h2d_bytes_per_step"] > 0 and d["e2e"]["d2h_bytes_per_step"] == 4
     assert d["config"]["workload"].startswith("llama3_head")
+    assert set(d["modes"]) == {"recompute", "stored"} and d["impl_config"]["mode"] == "kept"
+    m = d["memory"]
+    # The library allocates nothing; its scratch stays under the stated bound.
+    assert m["device_free_drop_during_step_mib"] == 0
+    assert m["scratch_mib"] <= m["scratch_bound_mib"]
+    assert abs(m["peak_extra_mib"] - m["scratch_mib"] - m["outputs_mib"]) < 1.0

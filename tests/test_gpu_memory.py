@@ -1,0 +1,60 @@
+"""Peak device memory of a forward + backward, measured, against the method's
+budget: one [N, BVc] 16-bit block (the dL staging block, which in the
+kept-block mode first holds the kept probabilities, plus their per-32-column
+maxima), the fp32 dx accumulator, the forward's per-vocabulary-tile partials
+and per-token coefficients. No [V, H] fp32 dW accumulator exists (dW is
+written once per block), and the library allocates nothing itself: the
+device's free memory does not move during a call."""
+import pytest
+import torch
+
+import linear_cross_entropy_gemm_gb300 as F
+from linear_cross_entropy_gemm_gb300 import inputs as I
+from linear_cross_entropy_gemm_gb300 import tuning
+from parity import DeviceProblem
+
+pytestmark = pytest.mark.gpu
+
+
+def scratch_bound(N, H, V, bv):
+    return (N * bv * 2 + N * (bv // 32) * 4 + N * H * 4 + N * -(-V // 256) * 12 + N * 32
+            + (1 << 20))
+
+
+@pytest.mark.parametrize("mode", ["recompute", "kept"])
+@pytest.mark.parametrize("name", ["tiny", "medium", "llama3_head", "large_logit", "vocab256k"])
+def test_peak_memory_within_the_block_budget(name, mode):
+    wl = I.WORKLOADS[name]
+    N, H, V = wl.N, wl.H, wl.V
+    dev = torch.device("cuda", 0)
+    p = DeviceProblem(I.make_inputs(wl))
+    p.run(mode=mode)  # first launches (module loading) outside the measurement
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    free0 = torch.cuda.mem_get_info(dev)[0]
+    reserved0 = torch.cuda.memory_reserved(dev)
+    out = p.run(mode=mode)
+    torch.cuda.synchronize(dev)
+    free1 = torch.cuda.mem_get_info(dev)[0]
+    reserved1 = torch.cuda.memory_reserved(dev)
+    assert out["err"] == 0
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    outputs = sum(t.numel() * t.element_size()
+                  for t in (out["loss"], out["lse"], out["dx"], out["dW"], out["db"])
+                  if t is not None)
+    bv = tuning.library_default_block(N, V)
+    bound = scratch_bound(N, H, V, bv)
+    assert peak - outputs <= bound, (peak - outputs, bound)
+    # Everything the device gave away during the call went to torch's pool:
+    # nothing was allocated behind the allocator's back.
+    assert (free0 - free1) == (reserved1 - reserved0)
+    # The kept-block mode takes no more memory than the recompute mode.
+    if mode == "kept":
+        kept = F.flce_kept_size(N, H, V)
+        ws = F.flce_workspace_size(N, H, V, "backward_keep", has_bias=wl.has_bias,
+                                   label_smoothing=wl.label_smoothing)
+        ws_plain = F.flce_workspace_size(N, H, V, "backward", has_bias=wl.has_bias,
+                                         label_smoothing=wl.label_smoothing)
+        assert kept + ws <= ws_plain + N * (bv // 32) * 4 + (1 << 10)
