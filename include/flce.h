@@ -304,6 +304,9 @@ flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_
  * rejected with FLCE_ERR_WORKSPACE_TOO_SMALL before anything runs.
  * The first call on each device looks up the array's device address with
  * that device current; make that first call before any stream capture.
+ * The address is kept for the life of the process, so do not use this entry
+ * point across a cudaDeviceReset of that device (the reset unloads the
+ * library's module and the kept address would no longer be the array's).
  * The call allocates and frees nothing. All calls share the one array, so
  * calls that overlap on the GPU (e.g. on two streams) race on it: order them.
  * Each call writes every scratch value it later reads, so stale contents from

@@ -33,7 +33,9 @@ void* g_scratch_dev[kMaxDevices] = {};
 
 // The name g_scratch is only a host-side handle; the device address comes
 // from cudaGetSymbolAddress, looked up once per device with that device
-// current (the first call on each device does it).
+// current (the first call on each device does it). The address is kept for
+// the life of the process: a cudaDeviceReset would invalidate it, and the
+// header tells callers not to use this entry point across one.
 flce_status_t scratch_for_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
