@@ -27,4 +27,5 @@ def test_c_program_against_closed_form(tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
-    assert r.stdout.startswith("ok")
+    lines = r.stdout.splitlines()
+    assert len(lines) == 2 and all(l.startswith("ok") for l in lines), r.stdout

@@ -1,6 +1,7 @@
-"""flce_forward + flce_backward captured into one CUDA graph: the calls make
-no host synchronisation or allocation of their own (the caller passes the
-workspace and outputs), so a replay runs the same kernels on the captured
+"""flce_forward + flce_backward captured into one CUDA graph, in the
+recompute and the kept-block modes: the calls make no host synchronisation
+or allocation of their own (the caller passes the workspace, the kept
+buffer and the outputs), so a replay runs the same kernels on the captured
 buffers. The library is run-to-run deterministic, so a replay must equal an
 eager call bit for bit, also after the inputs are overwritten in place."""
 import pytest
@@ -20,8 +21,9 @@ def _problem(seed):
     return wl, inp
 
 
+@pytest.mark.parametrize("mode", ["recompute", "kept"])
 @pytest.mark.parametrize("form", ["single", "pair", "wide"])
-def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form):
+def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form, mode):
     wl, inp = _problem(41)
     dev = torch.device("cuda:0")
     x = bf16_dev(inp.x, dev)
@@ -33,8 +35,12 @@ def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form):
     N, H, V = wl.N, wl.H, wl.V
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", has_bias=True, **opts),
                       dtype=torch.uint8, device=dev)
-    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward", has_bias=True, **opts),
+    keep = mode == "kept"
+    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward_keep" if keep else "backward",
+                                            has_bias=True, bwd_vocab_block=1024, **opts),
                       dtype=torch.uint8, device=dev)
+    kept = (torch.empty(F.flce_kept_size(N, H, V, bwd_vocab_block=1024), dtype=torch.uint8,
+                        device=dev) if keep else None)
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dx = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
@@ -42,9 +48,10 @@ def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form):
     db = torch.empty(V, dtype=torch.float32, device=dev)
 
     def step():
-        F.flce_forward(x, W, b, y, workspace=fws, out=(loss, lse), gemm_form=form, **opts)
+        F.flce_forward(x, W, b, y, workspace=fws, out=(loss, lse), gemm_form=form, kept=kept,
+                       bwd_vocab_block=1024, **opts)
         F.flce_backward(dloss, lse, x, W, b, y, workspace=bws, out=(dx, dW, db),
-                        gemm_form=form, **opts)
+                        gemm_form=form, kept=kept, bwd_vocab_block=1024, **opts)
 
     def snapshot():
         torch.cuda.synchronize(dev)
