@@ -304,7 +304,7 @@ class Problem:
         b = {"mode": mode}
         b["fws"] = torch.empty(F.flce_workspace_size(N, H, V, "forward", **self.opts),
                                dtype=torch.uint8, device=dev)
-        kind = "backward_keep" if mode == "kept" else "backward"
+        kind = {"kept": "backward_keep", "stored": "backward_store"}.get(mode, "backward")
         b["bws"] = torch.empty(F.flce_workspace_size(N, H, V, kind, bwd_vocab_block=bvb,
                                                      has_bias=wl.has_bias, **self.opts),
                                dtype=torch.uint8, device=dev)

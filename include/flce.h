@@ -135,16 +135,15 @@ typedef struct {
 } flce_trace_t;
 
 /* Workspace bytes a call needs: which = 0 for the forward calls, 1 for
- * flce_backward (and the stored and shard backwards), 2 for
- * flce_backward_keep (no dL block: it stages dL in the kept buffer).
+ * flce_backward and flce_backward_shard, 2 for flce_backward_keep (no dL
+ * block: it stages dL in the kept buffer), 3 for flce_backward_store.
  * Returns 0 for invalid parameters or N == 0. */
 size_t flce_workspace_size(const flce_params_t* p, int which);
 
 /* The GEMM form (FLCE_GEMM_SINGLE_CTA, _CTA_PAIR or _WIDE_PAIR) that calls with
  * these parameters run for one GEMM: which = 0 the forward logits GEMM, 1 the
  * backward recompute, 2 dW, 3 dx (1 and 2 for the first vocabulary block).
- * The dx GEMM and the forward of flce_forward_store run a wide form as
- * CTA pairs. Host only; returns -1 for NULL, invalid parameters or an invalid
+ * The dx GEMM runs a wide form as CTA pairs. Host only; returns -1 for NULL, invalid parameters or an invalid
  * `which`. */
 int32_t flce_resolved_gemm_form(const flce_params_t* p, int32_t which);
 
@@ -188,30 +187,6 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
                                    flce_trace_t* trace);
 
 /*
- * Stored-probability mode: no logits recompute in the backward pass.
- * flce_forward_store computes what flce_forward does and also keeps, in the
- * caller's `saved` buffer (flce_saved_size(p) bytes, 16-byte aligned), every
- * logit's probability relative to its 128 x 256 tile's row maximum,
- * q = exp(z - m_t) in fp16, plus the maxima m_t (fp32). flce_backward_store
- * then forms dlogits = (1 + 2 lam lse) q exp(m_t - lse) - eps/V - (1 - eps)
- * delta_y from that state (an HBM pass) instead of recomputing x W^T, saving
- * 2 N H V flops (a quarter of the step) for 2 N V bytes of memory. `saved`
- * must be left untouched between the two calls; workspaces are as in the
- * plain calls (flce_workspace_size). trace may be NULL.
- */
-size_t flce_saved_size(const flce_params_t* p);
-flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const void* W,
-                                 const void* b, const int64_t* y, float* loss, float* lse,
-                                 void* saved, size_t saved_bytes, void* workspace,
-                                 size_t workspace_bytes, int32_t* dev_err, void* stream,
-                                 flce_trace_t* trace);
-flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss, const float* lse,
-                                  const void* saved, size_t saved_bytes, const void* x,
-                                  const void* W, const void* b, const int64_t* y, void* dx,
-                                  void* dW, void* db, void* workspace, size_t workspace_bytes,
-                                  int32_t* dev_err, void* stream, flce_trace_t* trace);
-
-/*
  * Kept-block mode: the backward recomputes every vocabulary block but the
  * first. (Our combination of DeepSpeed PR #8792 "What", where the backward
  * recomputes the logits one vocabulary block at a time into a staged block,
@@ -248,6 +223,29 @@ flce_status_t flce_backward_keep(const flce_params_t* p, const float* dloss, con
                                  const void* b, const int64_t* y, void* dx, void* dW, void* db,
                                  void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                  void* stream, flce_trace_t* trace);
+
+/*
+ * Stored-probability mode: no logits recompute in the backward pass. This is
+ * the kept-block mode with one block spanning the whole vocabulary
+ * (p->bwd_vocab_block is ignored): flce_forward_store keeps every logit's
+ * probability, ~2 N V bytes in `saved` (flce_saved_size(p) bytes, 16-byte
+ * aligned), and flce_backward_store converts it to dlogits in place and runs
+ * one dW and one dx GEMM over the whole vocabulary, saving 2 N H V flops (a
+ * quarter of the step) for that memory. Its workspace is
+ * flce_workspace_size(p, 3). The backward consumes `saved` (it holds dL
+ * afterwards); leave it untouched between the two calls. trace may be NULL.
+ */
+size_t flce_saved_size(const flce_params_t* p);
+flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const void* W,
+                                 const void* b, const int64_t* y, float* loss, float* lse,
+                                 void* saved, size_t saved_bytes, void* workspace,
+                                 size_t workspace_bytes, int32_t* dev_err, void* stream,
+                                 flce_trace_t* trace);
+flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss, const float* lse,
+                                  void* saved, size_t saved_bytes, const void* x,
+                                  const void* W, const void* b, const int64_t* y, void* dx,
+                                  void* dW, void* db, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_err, void* stream, flce_trace_t* trace);
 
 /*
  * Vocabulary-parallel FLCE (DeepSpeed PR #8792, "What": each rank holds a

@@ -99,9 +99,10 @@ class KernelTrace:
 
 
 def flce_workspace_size(N, H, V, which: str, **opts) -> int:
-    """Workspace bytes of a call: which = "forward", "backward" or
+    """Workspace bytes of a call: which = "forward", "backward",
     "backward_keep" (the backward of a kept-block forward, which stages dL in
-    the kept buffer and so needs no dL block of its own)."""
+    the kept buffer and so needs no dL block of its own) or "backward_store"
+    (the stored-probability backward)."""
     p = params(N, H, V, **opts)
     return int(_lib.load().flce_workspace_size(p, _lib.WORKSPACE_KIND[which]))
 
@@ -123,7 +124,8 @@ def resolved_gemm_form(N, H, V, gemm_form="default", gemm="fwd_lse", **opts) -> 
 
 def flce_saved_size(N, H, V, **opts) -> int:
     """Bytes of the state flce_forward(..., saved=) keeps for the stored-
-    probability backward (fp16 tile probabilities + tile maxima, ~2 N V bytes)."""
+    probability backward: every logit's fp16 probability relative to its
+    32-column chunk's running maximum, plus those maxima (~2.1 N V bytes)."""
     return int(_lib.load().flce_saved_size(params(N, H, V, **opts)))
 
 
@@ -241,7 +243,7 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
         db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
     if saved is not None and kept is not None:
         raise ValueError("flce: give saved= or kept=, not both")
-    need = lib.flce_workspace_size(p, 2 if kept is not None else 1)
+    need = lib.flce_workspace_size(p, 2 if kept is not None else 3 if saved is not None else 1)
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
     if saved is not None or kept is not None:

@@ -59,7 +59,7 @@ class FlceTrace(ctypes.Structure):
 KERNEL_NAMES = ("fwd_lse", "fwd_merge", "fwd_finalize", "bwd_prep", "bwd_dlogits", "bwd_db",
                 "bwd_dw", "bwd_dx", "bwd_convert")
 # flce_workspace_size's `which`.
-WORKSPACE_KIND = {"forward": 0, "backward": 1, "backward_keep": 2}
+WORKSPACE_KIND = {"forward": 0, "backward": 1, "backward_keep": 2, "backward_store": 3}
 
 
 class FlceError(RuntimeError):

@@ -326,87 +326,6 @@ struct FwdLseEpi {
   }
 };
 
-// --------------------------------------------- forward, keeping probabilities
-// As FwdLseEpi, and also writes q = 2^(z log2e - m_t) for every logit of the
-// tile as fp16 into probs[row, v] (m_t = the tile's row max, written to
-// part_m), so a later backward can form dL = a_n q 2^(m_t - lse2) - c_n - t_n [v == y]
-// without recomputing the logits. Two passes over the accumulator: the first
-// finds m_t (and z_y, sum z), the second exponentiates, sums and stores.
-struct FwdStoreArgs {
-  FwdLseArgs base;
-  __half* probs;  // [Ntok, ld_p]
-  int ld_p;       // tiles_v * 256
-};
-
-template <bool HAS_BIAS, bool HAS_SMOOTH>
-struct FwdStoreEpi {
-  static constexpr bool kAMN = false, kBMN = false;
-  // Two passes over the whole sub-tile: never column-split (it runs on pairs).
-  static constexpr int kWideWarps = 8, kStageNeed = 0;
-  using Args = FwdStoreArgs;
-  __device__ static void tile(const Args& A, const GemmGeom&, int tm, int tn, int row_in_tile,
-                              int, int, uint32_t taddr, void*, const EpiSlice&) {
-    const FwdLseArgs& a = A.base;
-    const int row = tm * kBM + row_in_tile;
-    const int v0 = tn * kBN;
-    const int64_t yv = row < a.Ntok ? __ldg(a.y + row) - a.y_off : -1;
-    const int ty = (yv >= v0 && yv < static_cast<int64_t>(v0) + kBN) ? static_cast<int>(yv - v0) : -1;
-    float m = -INFINITY, S = 0.f, zt = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float v[32], bv[32];
-      tmem_ld_32cols(taddr + c * 32, v);
-      const int col0 = v0 + c * 32;
-      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float z = (v[j] + bv[j]) * a.scale;
-        const bool ok = col0 + j < a.V;
-        if constexpr (HAS_SMOOTH) S += ok ? z : 0.f;
-        zt = (c * 32 + j == ty) ? z : zt;
-        m = ok ? fmaxf(m, z * kLog2e) : m;
-      }
-    }
-    float d = 0.f;
-    __half* prow = A.probs + static_cast<size_t>(row < a.Ntok ? row : 0) * A.ld_p + v0;
-#pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float v[32], bv[32];
-      tmem_ld_32cols(taddr + c * 32, v);
-      const int col0 = v0 + c * 32;
-      load_bias32<HAS_BIAS>(a.bias, col0 < a.V ? col0 : 0, a.V, bv, a.fp16 != 0);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float z = (v[j] + bv[j]) * a.scale;
-        const float q = (col0 + j < a.V) ? fast_exp2(fmaf(z, kLog2e, -m)) : 0.f;
-        d += q;
-        v[j] = q;
-      }
-      if (row < a.Ntok) {
-        uint4* dst = reinterpret_cast<uint4*>(prow + c * 32);
-#pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {
-          uint4 u;
-          uint32_t* w = reinterpret_cast<uint32_t*>(&u);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const __half2 h = __floats2half2_rn(v[qd * 8 + 2 * e], v[qd * 8 + 2 * e + 1]);
-            w[e] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          dst[qd] = u;
-        }
-      }
-    }
-    if (row < a.Ntok) {
-      const size_t o = static_cast<size_t>(tn) * a.Ntok + row;
-      a.part_m[o] = m;
-      a.part_d[o] = d;
-      if constexpr (HAS_SMOOTH) a.part_s[o] = S;
-      if (ty >= 0) a.zy[row] = zt;
-    }
-  }
-};
-
 // ------------------------------------------------- backward: recompute + dL
 // Recomputes a logits tile of the current vocab block, forms
 // dL = a_n p - c_n - t_n [v == y_n] with per-row coefficients

@@ -245,24 +245,6 @@ size_t carve_bwd(const flce_params_t* p, void* base, BwdWs* w, bool kept = false
   return c.used() + kAlign;
 }
 
-// State kept between flce_forward_store and flce_backward_store:
-// q [N, tiles_v * 256] fp16, then the tile maxima m_t [tiles_v, N] fp32.
-struct Saved {
-  __half* probs;
-  int ld_p;
-  float* part_m;
-};
-
-size_t carve_saved(const flce_params_t* p, void* base, Saved* sv) {
-  const size_t N = static_cast<size_t>(p->N);
-  const size_t NT = static_cast<size_t>(cdiv(p->V, kBN));
-  Carver c(base, 0);
-  sv->ld_p = static_cast<int>(NT * kBN);
-  sv->probs = c.take<__half>(N * NT * kBN);
-  sv->part_m = c.take<float>(NT * N);
-  return c.used() + kAlign;
-}
-
 // State kept between flce_forward_keep and flce_backward_keep: the first
 // backward vocabulary block's q [N, ld] (ld = BVc; the block's dL staging
 // buffer, converted in place) as fp16, then the running maxima of its
@@ -283,6 +265,15 @@ size_t carve_kept(const flce_params_t* p, void* base, Kept* k) {
   k->dq = c.take<uint16_t>(N * static_cast<size_t>(bv));
   k->kmax = c.take<float>(static_cast<size_t>(cdiv(k->cols, 32)) * N);
   return c.used() + kAlign;
+}
+
+// The stored-probability mode is the kept-block mode with one backward
+// vocabulary block spanning the whole vocabulary: every probability is kept
+// and nothing is recomputed.
+flce_params_t whole_vocab_block(const flce_params_t* p) {
+  flce_params_t q = *p;
+  q.bwd_vocab_block = (p->V + 255) / 256 * 256;
+  return q;
 }
 
 GemmGeom geom(int M, int N, int K, bool fp16) {
@@ -346,21 +337,21 @@ struct Tracer {
 
 }  // namespace
 
-// saved: the full stored-probability state; kept: the kept block. At most
-// one of them is given.
-static flce_status_t forward_impl(const flce_params_t* p, const void* x, const void* W,
-                                  const void* b, const int64_t* y, float* loss, float* lse,
-                                  void* saved, size_t saved_bytes, void* workspace,
-                                  size_t workspace_bytes, int32_t* dev_err, void* stream,
-                                  flce_trace_t* trace, float* shard_stats = nullptr,
-                                  void* kept = nullptr, size_t kept_bytes = 0);
-static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, const float* lse,
-                                   const void* saved, size_t saved_bytes, const void* x,
-                                   const void* W, const void* b, const int64_t* y, void* dx,
-                                   void* dW, void* db, void* workspace, size_t workspace_bytes,
-                                   int32_t* dev_err, void* stream, flce_trace_t* trace,
-                                   bool shard = false, void* kept = nullptr,
-                                   size_t kept_bytes = 0);
+// kept: the kept block (flce_forward_keep / flce_backward_keep, and the
+// stored mode with a block spanning the vocabulary); shard_stats / shard: the
+// vocabulary-shard calls. NVTX names the call by `name`.
+static flce_status_t forward_impl(const char* name, const flce_params_t* p, const void* x,
+                                  const void* W, const void* b, const int64_t* y, float* loss,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_err, void* stream, flce_trace_t* trace,
+                                  float* shard_stats = nullptr, void* kept = nullptr,
+                                  size_t kept_bytes = 0);
+static flce_status_t backward_impl(const char* name, const flce_params_t* p, const float* dloss,
+                                   const float* lse, const void* x, const void* W, const void* b,
+                                   const int64_t* y, void* dx, void* dW, void* db,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                   void* stream, flce_trace_t* trace, bool shard = false,
+                                   void* kept = nullptr, size_t kept_bytes = 0);
 
 extern "C" {
 
@@ -393,6 +384,11 @@ size_t flce_workspace_size(const flce_params_t* p, int which) {
     BwdWs w;
     return carve_bwd(p, nullptr, &w, which == 2);
   }
+  if (which == 3) {
+    const flce_params_t q = whole_vocab_block(p);
+    BwdWs w;
+    return carve_bwd(&q, nullptr, &w, true);
+  }
   return 0;
 }
 
@@ -407,8 +403,8 @@ flce_status_t flce_forward_traced(const flce_params_t* p, const void* x, const v
                                   const void* b, const int64_t* y, float* loss, float* lse,
                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                   void* stream, flce_trace_t* trace) {
-  return forward_impl(p, x, W, b, y, loss, lse, nullptr, 0, workspace, workspace_bytes, dev_err,
-                      stream, trace);
+  return forward_impl("flce_forward", p, x, W, b, y, loss, lse, workspace, workspace_bytes,
+                      dev_err, stream, trace);
 }
 
 flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const void* W,
@@ -416,15 +412,18 @@ flce_status_t flce_forward_store(const flce_params_t* p, const void* x, const vo
                                  void* saved, size_t saved_bytes, void* workspace,
                                  size_t workspace_bytes, int32_t* dev_err, void* stream,
                                  flce_trace_t* trace) {
-  if (!saved && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
-  return forward_impl(p, x, W, b, y, loss, lse, saved, saved_bytes, workspace, workspace_bytes,
-                      dev_err, stream, trace);
+  if (!p) return FLCE_ERR_INVALID_ARG;
+  if (!saved && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  const flce_params_t q = whole_vocab_block(p);
+  return forward_impl("flce_forward_store", &q, x, W, b, y, loss, lse, workspace,
+                      workspace_bytes, dev_err, stream, trace, nullptr, saved, saved_bytes);
 }
 
 size_t flce_saved_size(const flce_params_t* p) {
-  if (check_params(p) != FLCE_OK || p->N == 0) return 0;
-  Saved sv{};  // filled by carve_saved when `saved` is given
-  return carve_saved(p, nullptr, &sv);
+  if (check_params(p) != FLCE_OK || p->N == 0 || !whole_vocab(p)) return 0;
+  const flce_params_t q = whole_vocab_block(p);
+  Kept k{};
+  return carve_kept(&q, nullptr, &k);
 }
 
 size_t flce_kept_size(const flce_params_t* p) {
@@ -439,22 +438,18 @@ flce_status_t flce_forward_keep(const flce_params_t* p, const void* x, const voi
                                 size_t workspace_bytes, int32_t* dev_err, void* stream,
                                 flce_trace_t* trace) {
   if (!kept && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
-  return forward_impl(p, x, W, b, y, loss, lse, nullptr, 0, workspace, workspace_bytes, dev_err,
-                      stream, trace, nullptr, kept, kept_bytes);
+  return forward_impl("flce_forward_keep", p, x, W, b, y, loss, lse, workspace, workspace_bytes,
+                      dev_err, stream, trace, nullptr, kept, kept_bytes);
 }
 
 }  // extern "C"
 
-static flce_status_t forward_impl(const flce_params_t* p, const void* x, const void* W,
-                                  const void* b, const int64_t* y, float* loss, float* lse,
-                                  void* saved, size_t saved_bytes, void* workspace,
-                                  size_t workspace_bytes, int32_t* dev_err, void* stream,
-                                  flce_trace_t* trace, float* shard_stats, void* kept,
-                                  size_t kept_bytes) {
-  NvtxRange nvtx_range(shard_stats ? "flce_forward_shard"
-                       : saved     ? "flce_forward_store"
-                       : kept      ? "flce_forward_keep"
-                                   : "flce_forward");
+static flce_status_t forward_impl(const char* name, const flce_params_t* p, const void* x,
+                                  const void* W, const void* b, const int64_t* y, float* loss,
+                                  float* lse, void* workspace, size_t workspace_bytes,
+                                  int32_t* dev_err, void* stream, flce_trace_t* trace,
+                                  float* shard_stats, void* kept, size_t kept_bytes) {
+  NvtxRange nvtx_range(name);
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
   if (shard_stats) {
@@ -476,14 +471,9 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   FwdWs w;
   const size_t need = carve_fwd(p, nullptr, &w);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  Saved sv{};  // filled by carve_saved when `saved` is given
-  if (saved) {
-    if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-    if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
-  }
   Kept kp{};  // filled by carve_kept when `kept` is given
   if (kept) {
-    if (saved || shard_stats) return FLCE_ERR_INVALID_ARG;
+    if (shard_stats) return FLCE_ERR_INVALID_ARG;
     if (kept_bytes < carve_kept(p, nullptr, &kp)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(kept)) return FLCE_ERR_ALIGNMENT;
   }
@@ -491,10 +481,6 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
   if ((st = device_info(&sms)) != FLCE_OK) return st;
   carve_fwd(p, workspace, &w);
   if (kept) carve_kept(p, kept, &kp);
-  if (saved) {
-    carve_saved(p, saved, &sv);
-    w.part_m = sv.part_m;  // the tile maxima are part of the saved state
-  }
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
   const GemmKind kind = gemm_for(gemm_kind(p), p->N, p->V, p->H);
@@ -531,18 +517,9 @@ static flce_status_t forward_impl(const flce_params_t* p, const void* x, const v
     if (!encode_store_2d(&ea.keep_map, kp.dq, kp.cols, N, static_cast<uint64_t>(kp.ld) * 2, false))
       return FLCE_ERR_CUDA;
   }
-  cudaError_t le;
-  if (saved) {
-    FwdStoreArgs sa;
-    sa.base = ea;
-    sa.probs = sv.probs;
-    sa.ld_p = sv.ld_p;
-    le = launch_fwd_store(kind, mx, mw, g, sa, p->has_bias != 0, p->label_smoothing > 0.f,
-                          reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
-  } else {
-    le = launch_fwd_lse(kind, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
-                        kept != nullptr, reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
-  }
+  const cudaError_t le =
+      launch_fwd_lse(kind, mx, mw, g, ea, p->has_bias != 0, p->label_smoothing > 0.f,
+                     kept != nullptr, reinterpret_cast<int*>(dev_err), grid_for(g, sms), s);
   if (le != cudaSuccess || !tr.after(FLCE_KERNEL_FWD_LSE)) return FLCE_ERR_CUDA;
 
   if (shard_stats) {
@@ -608,7 +585,7 @@ extern "C" flce_status_t flce_backward_traced(const flce_params_t* p, const floa
                                               void* db, void* workspace, size_t workspace_bytes,
                                               int32_t* dev_err, void* stream,
                                               flce_trace_t* trace) {
-  return backward_impl(p, dloss, lse, nullptr, 0, x, W, b, y, dx, dW, db, workspace,
+  return backward_impl("flce_backward", p, dloss, lse, x, W, b, y, dx, dW, db, workspace,
                        workspace_bytes, dev_err, stream, trace);
 }
 
@@ -619,32 +596,31 @@ extern "C" flce_status_t flce_backward_keep(const flce_params_t* p, const float*
                                             void* workspace, size_t workspace_bytes,
                                             int32_t* dev_err, void* stream, flce_trace_t* trace) {
   if (!kept && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
-  return backward_impl(p, dloss, lse, nullptr, 0, x, W, b, y, dx, dW, db, workspace,
+  return backward_impl("flce_backward_keep", p, dloss, lse, x, W, b, y, dx, dW, db, workspace,
                        workspace_bytes, dev_err, stream, trace, false, kept, kept_bytes);
 }
 
 extern "C" flce_status_t flce_backward_store(const flce_params_t* p, const float* dloss,
-                                             const float* lse, const void* saved,
-                                             size_t saved_bytes, const void* x, const void* W,
-                                             const void* b, const int64_t* y, void* dx, void* dW,
-                                             void* db, void* workspace, size_t workspace_bytes,
+                                             const float* lse, void* saved, size_t saved_bytes,
+                                             const void* x, const void* W, const void* b,
+                                             const int64_t* y, void* dx, void* dW, void* db,
+                                             void* workspace, size_t workspace_bytes,
                                              int32_t* dev_err, void* stream,
                                              flce_trace_t* trace) {
-  if (!saved && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
-  return backward_impl(p, dloss, lse, saved, saved_bytes, x, W, b, y, dx, dW, db, workspace,
-                       workspace_bytes, dev_err, stream, trace);
+  if (!p) return FLCE_ERR_INVALID_ARG;
+  if (!saved && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  const flce_params_t q = whole_vocab_block(p);
+  return backward_impl("flce_backward_store", &q, dloss, lse, x, W, b, y, dx, dW, db, workspace,
+                       workspace_bytes, dev_err, stream, trace, false, saved, saved_bytes);
 }
 
-static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, const float* lse,
-                                   const void* saved, size_t saved_bytes, const void* x,
-                                   const void* W, const void* b, const int64_t* y, void* dx,
-                                   void* dW, void* db, void* workspace, size_t workspace_bytes,
-                                   int32_t* dev_err, void* stream, flce_trace_t* trace,
-                                   bool shard, void* kept, size_t kept_bytes) {
-  NvtxRange nvtx_range(shard   ? "flce_backward_shard"
-                       : saved ? "flce_backward_store"
-                       : kept  ? "flce_backward_keep"
-                               : "flce_backward");
+static flce_status_t backward_impl(const char* name, const flce_params_t* p, const float* dloss,
+                                   const float* lse, const void* x, const void* W, const void* b,
+                                   const int64_t* y, void* dx, void* dW, void* db,
+                                   void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                   void* stream, flce_trace_t* trace, bool shard, void* kept,
+                                   size_t kept_bytes) {
+  NvtxRange nvtx_range(name);
   flce_status_t st = check_params(p);
   if (st != FLCE_OK) return st;
   if (shard ? p->vocab_total == 0 : !whole_vocab(p)) return FLCE_ERR_INVALID_ARG;
@@ -666,15 +642,9 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
   BwdWs w;
   const size_t need = carve_bwd(p, nullptr, &w, kept != nullptr);
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  Saved sv{};  // filled by carve_saved when `saved` is given
-  if (saved) {
-    if (saved_bytes < carve_saved(p, nullptr, &sv)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-    if (!aligned16(saved)) return FLCE_ERR_ALIGNMENT;
-    carve_saved(p, const_cast<void*>(saved), &sv);
-  }
   Kept kp{};  // filled by carve_kept when `kept` is given
   if (kept) {
-    if (saved || shard) return FLCE_ERR_INVALID_ARG;
+    if (shard) return FLCE_ERR_INVALID_ARG;
     if (kept_bytes < carve_kept(p, nullptr, &kp)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(kept)) return FLCE_ERR_ALIGNMENT;
     carve_kept(p, kept, &kp);
@@ -728,43 +698,21 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
         !encode_2d(&mdl_mn, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, 64, kBK, f16))
       return FLCE_ERR_CUDA;
 
-    // Recompute the block's logits (or read the stored or kept
+    // Recompute the block's logits (or, for the kept block, read the kept
     // probabilities) and form dL (bf16) and db partials.
     int db_parts = 0;
     const bool from_kept = kept && blk == 0;
     if (from_kept) {
       // In place: the kept q of block 0 becomes its dL.
       ConvertArgs ca;
-      ca.probs = reinterpret_cast<const __half*>(kp.dq);
-      ca.ld_p = static_cast<int>(kp.ld);
-      ca.part_m = kp.kmax;
-      ca.chunk_max = 1;
+      ca.q = reinterpret_cast<const __half*>(kp.dq);
+      ca.ld_q = static_cast<int>(kp.ld);
+      ca.chunk_max = kp.kmax;
       ca.coef = w.coef;
       ca.y = y;
       ca.y_off = p->vocab_start;
       ca.N = N;
       ca.v0 = 0;
-      ca.Vb = Vb;
-      ca.dL = w.dL;
-      ca.ld_dL = static_cast<int>(bv);
-      ca.fp16 = p->input_fp16;
-      ca.dl_scale = w.dl_scale;
-      ca.db_part = w.db_part;
-      ca.ld_db = static_cast<int>(bv);
-      if (launch_convert(ca, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_CONVERT))
-        return FLCE_ERR_CUDA;
-      db_parts = convert_db_parts(N);
-    } else if (saved) {
-      ConvertArgs ca;
-      ca.probs = sv.probs;
-      ca.ld_p = sv.ld_p;
-      ca.part_m = sv.part_m;
-      ca.chunk_max = 0;
-      ca.coef = w.coef;
-      ca.y = y;
-      ca.y_off = p->vocab_start;
-      ca.N = N;
-      ca.v0 = v0;
       ca.Vb = Vb;
       ca.dL = w.dL;
       ca.ld_dL = static_cast<int>(bv);
@@ -795,7 +743,7 @@ static flce_status_t backward_impl(const flce_params_t* p, const float* dloss, c
     da.ld_db = static_cast<int>(bv);
     if (!encode_store_2d(&da.dl_map, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, false))
       return FLCE_ERR_CUDA;
-    if (!saved && !from_kept) {
+    if (!from_kept) {
       if (launch_dlogits(gemm_for(kind, N, Vb, H), mx_k, mw_k, g1, da, p->has_bias != 0, derr,
                          grid_for(g1, sms),
                          s) != cudaSuccess ||
@@ -858,8 +806,8 @@ flce_status_t flce_forward_shard(const flce_params_t* p, const void* x, const vo
                                  const void* b, const int64_t* y, float* stats, void* workspace,
                                  size_t workspace_bytes, int32_t* dev_err, void* stream) {
   if (!stats && p && p->N > 0) return FLCE_ERR_INVALID_ARG;
-  return forward_impl(p, x, W, b, y, nullptr, nullptr, nullptr, 0, workspace, workspace_bytes,
-                      dev_err, stream, nullptr, stats);
+  return forward_impl("flce_forward_shard", p, x, W, b, y, nullptr, nullptr, workspace,
+                      workspace_bytes, dev_err, stream, nullptr, stats);
 }
 
 flce_status_t flce_shard_rescale(const flce_params_t* p, float* stats, const float* global_max,
@@ -922,8 +870,8 @@ flce_status_t flce_backward_shard(const flce_params_t* p, const float* dloss, co
                                   const void* x, const void* W, const void* b, const int64_t* y,
                                   float* dx_partial, void* dW, void* db, void* workspace,
                                   size_t workspace_bytes, int32_t* dev_err, void* stream) {
-  return backward_impl(p, dloss, lse, nullptr, 0, x, W, b, y, dx_partial, dW, db, workspace,
-                       workspace_bytes, dev_err, stream, nullptr, true);
+  return backward_impl("flce_backward_shard", p, dloss, lse, x, W, b, y, dx_partial, dW, db,
+                       workspace, workspace_bytes, dev_err, stream, nullptr, true);
 }
 
 flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_fp16,

@@ -137,19 +137,6 @@ cudaError_t launch_fwd_lse(GemmKind kind, const CUtensorMap& a, const CUtensorMa
                                         st);
 }
 
-cudaError_t launch_fwd_store(GemmKind form, const CUtensorMap& a, const CUtensorMap& b,
-                             const GemmGeom& g, const FwdStoreArgs& ea, bool has_bias,
-                             bool has_smooth, int* dev_err, int grid, cudaStream_t st) {
-  // The storing epilogue (two passes over the accumulator, 512 B of fp16 per
-  // row per 256 columns) is too long to leave exposed between wide tiles.
-  const GemmKind kind = form == kGemmWide ? kGemmPair : form;
-  if (has_bias)
-    return has_smooth ? launch_any<FwdStoreEpi<true, true>>(kind, a, b, g, ea, dev_err, grid, st)
-                      : launch_any<FwdStoreEpi<true, false>>(kind, a, b, g, ea, dev_err, grid, st);
-  return has_smooth ? launch_any<FwdStoreEpi<false, true>>(kind, a, b, g, ea, dev_err, grid, st)
-                    : launch_any<FwdStoreEpi<false, false>>(kind, a, b, g, ea, dev_err, grid, st);
-}
-
 cudaError_t launch_dlogits(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
                            const GemmGeom& g, const DlogitsArgs& ea, bool has_bias, int* dev_err,
                            int grid, cudaStream_t st) {

@@ -72,21 +72,20 @@ struct PrepArgs {
 };
 cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st);
 
-// Stored-probability backward: fp16 q [N, ld_p] and its maxima -> bf16 dL
-// block [N, ld_dL] and db partials [ceil(N/32), ld_db]. The maxima are per
-// 256-column tile (part_m [tiles_v, N], chunk_max = 0) or per 32-column chunk
-// of the block (part_m [ceil(Vb/32), N], chunk_max = 1; then probs may be dL:
-// the kept block converts in place).
+// Kept-probability backward (the kept block, and the stored mode, whose kept
+// block spans the vocabulary): fp16 q [N, ld_q] relative to the running
+// maxima of 32-column chunks chunk_max [ceil(Vb / 32), N] -> dL block
+// [N, ld_dL] (bf16, or fp16 when fp16 = 1) and db partials
+// [ceil(N / 32), ld_db]. q and dL may be the same buffer (converted in place).
 struct ConvertArgs {
-  const __half* probs;
-  int ld_p;
-  const float* part_m;
-  int chunk_max;
+  const __half* q;
+  int ld_q;
+  const float* chunk_max;
   const float4* coef;
   const int64_t* y;
   int64_t y_off;
   int N, v0, Vb;
-  uint16_t* dL;    // bf16 or fp16 (fp16 = 1)
+  uint16_t* dL;
   int ld_dL;
   int fp16;
   const float* dl_scale;
@@ -95,11 +94,6 @@ struct ConvertArgs {
 };
 cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st);
 int convert_db_parts(int N);
-
-struct FwdStoreArgs;
-cudaError_t launch_fwd_store(GemmKind kind, const CUtensorMap& a, const CUtensorMap& b,
-                             const GemmGeom& g, const FwdStoreArgs& ea, bool has_bias,
-                             bool has_smooth, int* dev_err, int grid, cudaStream_t st);
 
 // Vocabulary shards: local partials -> stats [4, N] = (m2, d, z_y or 0, sum z);
 // rescale d by 2^(m2 - M) against the all-shard max M; fp32 -> bf16 cast.

@@ -248,25 +248,22 @@ cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, 
   return cudaGetLastError();
 }
 
-// Stored-probability backward: dL[n, v] = a_n q[n, v] 2^(m(n, v) - lse2_n)
+// Kept-probability backward: dL[n, v] = a_n q[n, v] 2^(m_c(n, v) - lse2_n)
 //   - c_n - t_n [v == y_n] for the vocab block [v0, v0 + Vb), q being the
-// forward's fp16 2^(z log2e - m). One CTA covers 32 tokens x one 256-column
-// vocab tile. Thread i owns 8 columns (16-byte loads and stores) of rows
-// i/32, i/32 + 4, ..., so eight independent loads are in flight per thread;
-// the fp32 column sums over the 32 tokens (db partials, row blockIdx.y) are
-// combined through shared memory.
-//   kChunkMax = false: m is the maximum of the row's 256-column tile
-//     (part_m [tiles_v, N]; flce_forward_store's full saved state);
-//   kChunkMax = true: m is the running maximum of the row's 32-column chunk
-//     (part_m [ceil(Vb / 32), N]; the kept block of flce_forward_keep, which
-//     is converted in place: probs and dL are the same buffer, so q is read
-//     with plain loads).
+// forward's fp16 2^(z log2e - m_c) and m_c the running maximum of the row's
+// logits after the 32-column chunk that holds v (flce_forward_keep). One CTA
+// covers 32 tokens x one 256-column vocab tile. Thread i owns 8 columns
+// (16-byte loads and stores; one chunk) of rows i/32, i/32 + 4, ..., so
+// eight independent loads are in flight per thread; the fp32 column sums over
+// the 32 tokens (db partials, row blockIdx.y) are combined through shared
+// memory. The conversion runs in place (q and dL are the same buffer), so q is
+// read with plain loads: each thread reads its 16 bytes before it overwrites
+// them and no other thread touches them.
 constexpr int kConvRows = 32;
 constexpr int kConvRowGroups = 4;  // 128 threads = 32 column groups x 4 row groups
-template <bool kChunkMax>
 __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs a) {
-  // Per row: the factor a 2^(m - lse2) for the tile (kChunkMax: per chunk).
-  __shared__ float s_scale[kChunkMax ? 8 : 1][kConvRows];
+  // Per (chunk, row): the factor a 2^(m_c - lse2).
+  __shared__ float s_scale[8][kConvRows];
   __shared__ float s_c[kConvRows], s_t[kConvRows];
   __shared__ int s_ty[kConvRows];
   __shared__ float s_sum[kConvRowGroups][256];
@@ -283,21 +280,15 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
       const float4 cf = a.coef[r];
       c = cf.z;
       t = cf.w;
-      if constexpr (!kChunkMax) {
-        const float mt = a.part_m[static_cast<size_t>(a.v0 / 256 + tile) * a.N + r];
-        s_scale[0][threadIdx.x] = cf.y * exp2f(mt - cf.x);
-      }
       const int64_t yv = a.y[r] - a.y_off;
       const int64_t lo = static_cast<int64_t>(a.v0) + tile * 256;
       if (yv >= lo && yv < lo + 256) ty = static_cast<int>(yv - a.v0);
-    } else if constexpr (!kChunkMax) {
-      s_scale[0][threadIdx.x] = 0.f;
     }
     s_c[threadIdx.x] = c;
     s_t[threadIdx.x] = t;
     s_ty[threadIdx.x] = ty;
   }
-  if constexpr (kChunkMax) {
+  {
     // 8 chunks x 32 rows of maxima, two per thread (each chunk's 32 rows are
     // one coalesced 128-byte load).
     const int nchunks = (a.Vb + 31) / 32;
@@ -309,7 +300,7 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
       float sc = 0.f;
       if (r < a.N && cidx < nchunks) {
         const float4 cf = a.coef[r];
-        sc = cf.y * exp2f(a.part_m[static_cast<size_t>(cidx) * a.N + r] - cf.x);
+        sc = cf.y * exp2f(a.chunk_max[static_cast<size_t>(cidx) * a.N + r] - cf.x);
       }
       s_scale[ch][rr] = sc;
     }
@@ -324,18 +315,16 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
 #pragma unroll
   for (int k = 0; k < kConvRows / kConvRowGroups; ++k) {
     const int i = rg + kConvRowGroups * k;
-    if (r0 + i < a.N && colb < a.Vb) {
-      const uint4* src = reinterpret_cast<const uint4*>(
-          a.probs + static_cast<size_t>(r0 + i) * a.ld_p + a.v0 + colb);
-      q[k] = kChunkMax ? *src : __ldg(src);
-    }
+    if (r0 + i < a.N && colb < a.Vb)
+      q[k] = *reinterpret_cast<const uint4*>(a.q + static_cast<size_t>(r0 + i) * a.ld_q + a.v0 +
+                                             colb);
   }
 #pragma unroll
   for (int k = 0; k < kConvRows / kConvRowGroups; ++k) {
     const int i = rg + kConvRowGroups * k;
     if (r0 + i >= a.N || colb >= a.Vb) continue;
     const uint32_t w[4] = {q[k].x, q[k].y, q[k].z, q[k].w};
-    const float scale = s_scale[kChunkMax ? cg >> 2 : 0][i];
+    const float scale = s_scale[cg >> 2][i];
     float d[8];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -372,10 +361,7 @@ __global__ void __launch_bounds__(128) probs_to_dlogits_kernel(const ConvertArgs
 
 cudaError_t launch_convert(const ConvertArgs& a, cudaStream_t st) {
   dim3 grid((a.Vb + 255) / 256, (a.N + kConvRows - 1) / kConvRows);
-  if (a.chunk_max)
-    probs_to_dlogits_kernel<true><<<grid, 128, 0, st>>>(a);
-  else
-    probs_to_dlogits_kernel<false><<<grid, 128, 0, st>>>(a);
+  probs_to_dlogits_kernel<<<grid, 128, 0, st>>>(a);
   return cudaGetLastError();
 }
 

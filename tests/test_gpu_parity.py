@@ -328,8 +328,8 @@ def test_no_writes_outside_caller_buffers(N, mode):
         assert bool((tail == 0xA5).all()), f"{what}: write past the end"
 
     nf = F.flce_workspace_size(N, wl.H, wl.V, "forward", **opts)
-    nb = F.flce_workspace_size(N, wl.H, wl.V, "backward_keep" if mode == "kept" else "backward",
-                               bwd_vocab_block=512, **opts)
+    kind = {"kept": "backward_keep", "stored": "backward_store"}.get(mode, "backward")
+    nb = F.flce_workspace_size(N, wl.H, wl.V, kind, bwd_vocab_block=512, **opts)
     wf, wb = guarded(nf), guarded(nb)
     state, ns, skw = None, 0, {}
     if mode == "stored":
