@@ -458,7 +458,7 @@ def run_ours(args):
     prob = Problem(torch, F, wl, dev, tdt, fkw, bkw)
     if args.autotune:
         res = tuning.autotune(prob.x, prob.W, prob.b, prob.y, dloss=prob.dloss, reps=3,
-                              **prob.opts)
+                              mode="kept" if args.mode == "kept" else "recompute", **prob.opts)
         fkw.update(res.config.forward_kwargs())
         bkw.update(res.config.backward_kwargs())
         tune = res.as_dict()

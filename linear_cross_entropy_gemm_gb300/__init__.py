@@ -385,7 +385,8 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
                 x2.detach(), weight.detach(), None if bias is None else bias.detach(), y2,
                 ignore_index=self.ignore_index, label_smoothing=self.label_smoothing,
                 lse_square_scale=self.lse_square_scale, logit_scale=self.logit_scale,
-                reduction=self.reduction).config
+                reduction=self.reduction,
+                mode="kept" if self.recompute and self.keep_block else "recompute").config
         return fused_linear_cross_entropy(
             x2, y2, weight, bias, self.ignore_index, self.label_smoothing,
             self.lse_square_scale, self.logit_scale, self.reduction, self.recompute, config,

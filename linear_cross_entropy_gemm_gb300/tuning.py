@@ -92,12 +92,13 @@ def select(forward_ms: Dict[str, float], backward_ms: Dict[Tuple[str, int], floa
 
 
 def problem_key(x, W, b, *, label_smoothing: float, dW_dtype, db_dtype,
-                budget_bytes: int) -> tuple:
+                budget_bytes: int, mode: str = "recompute") -> tuple:
     """What the timings depend on: device, sizes, operand type, bias, the
-    smoothing partial, the gradient output types and the staging budget."""
+    smoothing partial, the gradient output types, the staging budget and the
+    backward mode."""
     return (torch.cuda.get_device_name(x.device), int(x.shape[0]), int(x.shape[1]),
             int(W.shape[0]), str(x.dtype), b is not None, float(label_smoothing) > 0.0,
-            str(dW_dtype), str(db_dtype), int(budget_bytes))
+            str(dW_dtype), str(db_dtype), int(budget_bytes), mode)
 
 
 _CACHE: Dict[tuple, TuneResult] = {}
@@ -134,15 +135,21 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
              dW_dtype: torch.dtype = torch.float32, db_dtype: torch.dtype = torch.float32,
              forms: Sequence[str] = FORMS, vocab_blocks: Optional[Sequence[int]] = None,
              budget_bytes: int = DEFAULT_DL_BUDGET, reps: int = 3, warmup: int = 1,
-             use_cache: bool = True,
+             use_cache: bool = True, mode: str = "recompute",
              timer: Callable[[Callable[[], None], int, int], float] = _event_timer) -> TuneResult:
-    """Time flce_forward per GEMM form and flce_backward per (form, BVc) on
+    """Time flce_forward per GEMM form and the backward per (form, BVc) on
     these tensors and return the fastest configuration (cached per
-    ``problem_key``). Allocates one set of outputs and the largest workspace
-    the candidates need; synchronises the current stream."""
-    from . import flce_backward, flce_forward, flce_workspace_size
+    ``problem_key``). mode "recompute" times flce_backward alone; mode "kept"
+    times, per (form, BVc), the kept-block forward + backward pair (the kept
+    block is BVc wide, so the pair is what the block choice changes), and
+    backward_ms then holds those pair times. Allocates one set of outputs and
+    the largest workspace (and kept buffer) the candidates need; synchronises
+    the current stream."""
+    from . import flce_backward, flce_forward, flce_kept_size, flce_workspace_size
+    if mode not in ("recompute", "kept"):
+        raise ValueError(f"autotune: mode must be 'recompute' or 'kept', got {mode!r}")
     key = problem_key(x, W, b, label_smoothing=label_smoothing, dW_dtype=dW_dtype,
-                      db_dtype=db_dtype, budget_bytes=budget_bytes)
+                      db_dtype=db_dtype, budget_bytes=budget_bytes, mode=mode)
     if use_cache and key in _CACHE:
         return _CACHE[key]
     N, H = x.shape
@@ -158,11 +165,16 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
 
     ws_f = torch.empty(max(flce_workspace_size(N, H, V, "forward", **size_opts), 1),
                        dtype=torch.uint8, device=dev)
-    need_b = max(flce_workspace_size(N, H, V, "backward", bwd_vocab_block=bv,
-                                     dW_fp32=dW_dtype == torch.float32,
+    kept = mode == "kept"
+    need_b = max(flce_workspace_size(N, H, V, "backward_keep" if kept else "backward",
+                                     bwd_vocab_block=bv, dW_fp32=dW_dtype == torch.float32,
                                      db_fp32=db_dtype == torch.float32, **size_opts)
                  for bv in blocks)
     ws_b = torch.empty(max(need_b, 1), dtype=torch.uint8, device=dev)
+    kept_buf = None
+    if kept:
+        need_k = max(flce_kept_size(N, H, V, bwd_vocab_block=bv, **size_opts) for bv in blocks)
+        kept_buf = torch.empty(max(need_k, 1), dtype=torch.uint8, device=dev)
     loss = torch.empty(N if reduction == "none" else 1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dx = torch.empty(N, H, dtype=x.dtype, device=dev)
@@ -175,14 +187,24 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
             lambda form=form: flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse),
                                            gemm_form=form, **opts), reps, warmup)
     flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse), **opts)
+    def kept_pair(form, bv):
+        flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse), gemm_form=form, kept=kept_buf,
+                     bwd_vocab_block=bv, **opts)
+        flce_backward(dloss, lse, x, W, b, y, dW_dtype=dW_dtype, db_dtype=db_dtype,
+                      bwd_vocab_block=bv, workspace=ws_b, out=(dx, dW, db), gemm_form=form,
+                      kept=kept_buf, **opts)
+
     backward_ms = {}
     for form in forms:
         for bv in blocks:
-            backward_ms[(form, int(bv))] = timer(
-                lambda form=form, bv=bv: flce_backward(
+            if kept:
+                fn = lambda form=form, bv=int(bv): kept_pair(form, bv)
+            else:
+                fn = lambda form=form, bv=int(bv): flce_backward(
                     dloss, lse, x, W, b, y, dW_dtype=dW_dtype, db_dtype=db_dtype,
-                    bwd_vocab_block=int(bv), workspace=ws_b, out=(dx, dW, db),
-                    gemm_form=form, **opts), reps, warmup)
+                    bwd_vocab_block=bv, workspace=ws_b, out=(dx, dW, db),
+                    gemm_form=form, **opts)
+            backward_ms[(form, int(bv))] = timer(fn, reps, warmup)
     result = TuneResult(config=select(forward_ms, backward_ms), forward_ms=forward_ms,
                         backward_ms=backward_ms, key=key)
     if use_cache:

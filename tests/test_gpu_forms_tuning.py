@@ -93,13 +93,14 @@ def _device_inputs(wl):
     return inp, x, W, b, y, dloss
 
 
-def test_autotune_picks_a_candidate_and_its_results_match_the_oracle():
+@pytest.mark.parametrize("mode", ["recompute", "kept"])
+def test_autotune_picks_a_candidate_and_its_results_match_the_oracle(mode):
     wl = I.Workload("tune", N=1000, H=512, V=5000, seed=34, b_std=0.05, ignore_frac=0.05,
                     label_smoothing=0.1, lse_square_scale=1e-4)
     inp, x, W, b, y, dloss = _device_inputs(wl)
     opts = opts_of(wl)
     tuning.clear_cache()
-    res = tuning.autotune(x, W, b, y, dloss=dloss, reps=2, **opts)
+    res = tuning.autotune(x, W, b, y, dloss=dloss, reps=2, mode=mode, **opts)
     blocks = tuning.vocab_block_candidates(wl.N, wl.V)
     assert set(res.forward_ms) == set(tuning.FORMS)
     assert set(res.backward_ms) == {(f, bv) for f in tuning.FORMS for bv in blocks}
@@ -107,10 +108,17 @@ def test_autotune_picks_a_candidate_and_its_results_match_the_oracle():
     cfg = res.config
     assert cfg.fwd_gemm_form in tuning.FORMS and cfg.bwd_gemm_form in tuning.FORMS
     assert cfg.bwd_vocab_block in blocks
-    assert tuning.autotune(x, W, b, y, dloss=dloss, **opts) is res  # cached per key
+    assert tuning.autotune(x, W, b, y, dloss=dloss, mode=mode, **opts) is res  # cached per key
 
-    loss, lse = F.flce_forward(x, W, b, y, **opts, **cfg.forward_kwargs())
-    dx, dW, db = F.flce_backward(dloss, lse, x, W, b, y, **opts, **cfg.backward_kwargs())
+    kept = None
+    if mode == "kept":
+        kept = torch.empty(F.flce_kept_size(wl.N, wl.H, wl.V,
+                                            bwd_vocab_block=cfg.bwd_vocab_block),
+                           dtype=torch.uint8, device=x.device)
+    loss, lse = F.flce_forward(x, W, b, y, kept=kept, bwd_vocab_block=cfg.bwd_vocab_block,
+                               **opts, **cfg.forward_kwargs())
+    dx, dW, db = F.flce_backward(dloss, lse, x, W, b, y, kept=kept, **opts,
+                                 **cfg.backward_kwargs())
     torch.cuda.synchronize()
     assert F.flce_read_device_error() == 0
     x64, W64, b64 = f64(inp)
