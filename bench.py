@@ -552,9 +552,10 @@ def run_ours(args):
     budget = {
         # The library's scratch bound: one [N, BVc] 16-bit block (dL staging,
         # or the kept probabilities) and the kept block's per-32-column maxima,
-        # the fp32 dx accumulator, the forward's per-tile partials and the
-        # per-token coefficients.
+        # the fp32 dx accumulator, the db column partials (with a bias), the
+        # forward's per-tile partials and the per-token coefficients.
         "scratch_bound_mib": (N * bv_used * 2 + N * (bv_used // 32) * 4 + N * H * 4
+                              + (4 * -(-N // 128) * bv_used * 4 if wl.has_bias else 0)
                               + N * -(-V // 256) * 12 + N * 32) / 2**20 + 1,
         # The same with the stated reading of "one [N, BV] tile set plus the
         # fp32 dW accumulator": the dL block and a [V, H] fp32 dW.
