@@ -2,9 +2,10 @@
 budget: one [N, BVc] 16-bit block (the dL staging block, which in the
 kept-block mode first holds the kept probabilities, plus their per-32-column
 maxima), the fp32 dx accumulator, the db column partials (with a bias), the
-forward's per-vocabulary-tile partials and per-token coefficients. No [V, H] fp32 dW accumulator exists (dW is
-written once per block), and the library allocates nothing itself: the
-device's free memory does not move during a call."""
+forward's per-vocabulary-tile partials and per-token coefficients. No [V, H]
+fp32 dW accumulator exists (dW is written once per block), and the library
+allocates nothing itself: the device's free memory does not move during a
+call."""
 import pytest
 import torch
 
