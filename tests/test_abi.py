@@ -133,3 +133,50 @@ def test_header_compiles_as_plain_c_and_cpp(tmp_path, lang, std):
     r = subprocess.run([cc, std, "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
                         "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_kept_and_stored_sizes(lib):
+    # The kept state is one [N, BVc] fp16 block plus fp32 maxima per 32
+    # columns; the kept backward's workspace is the plain backward's without
+    # its dL block; the stored state is the kept state of a block spanning V.
+    N, H, V = 8192, 4096, 128256
+    p = _lib.params(N, H, V)
+    bv = 65536  # the library default at N = 8192 (1 GiB of 16-bit dL)
+    kept = lib.flce_kept_size(p)
+    assert N * bv * 2 + N * (bv // 32) * 4 <= kept <= N * bv * 2 + N * (bv // 32) * 4 + 1024
+    assert lib.flce_workspace_size(p, 1) - lib.flce_workspace_size(p, 2) >= N * bv * 2
+    vr = (V + 255) // 256 * 256
+    saved = lib.flce_saved_size(p)
+    assert N * vr * 2 + N * (-(-V // 32)) * 4 <= saved <= N * vr * 2 + N * (-(-V // 32)) * 4 + 1024
+    # one block over the vocabulary: no dx accumulator, no dL block
+    assert lib.flce_workspace_size(p, 3) < lib.flce_workspace_size(p, 2)
+    assert lib.flce_workspace_size(p, 4) == 0
+    assert lib.flce_kept_size(_lib.params(0, 64, 10)) == 0
+    # a vocabulary shard has no kept or stored mode
+    assert lib.flce_kept_size(_lib.params(4, 64, 10, vocab_start=10, vocab_total=40)) == 0
+
+
+def test_kept_entry_points_reject_bad_arguments_on_host(lib):
+    p = _lib.params(4, 64, 1000, bwd_vocab_block=256)
+    f = ctypes.c_void_p(4096)  # never dereferenced: rejected before any launch
+    need = lib.flce_kept_size(p)
+    ws = 1 << 30
+    # no kept buffer
+    assert lib.flce_forward_keep(p, f, f, None, f, f, f, None, need, f, ws, None, None,
+                                 None) == 1
+    # too small, misaligned
+    assert lib.flce_forward_keep(p, f, f, None, f, f, f, f, need - 1, f, ws, None, None,
+                                 None) == 3
+    assert lib.flce_forward_keep(p, f, f, None, f, f, f, ctypes.c_void_p(4104), need, f, ws,
+                                 None, None, None) == 2
+    assert lib.flce_backward_keep(p, f, f, f, need - 1, f, f, None, f, f, f, None, f, ws,
+                                  None, None, None) == 3
+    # the kept backward's workspace must hold its (dL-free) carving
+    assert lib.flce_backward_keep(p, f, f, f, need, f, f, None, f, f, f, None, f, 16, None,
+                                  None, None) == 3
+    # stored mode: state too small
+    ns = lib.flce_saved_size(p)
+    assert lib.flce_forward_store(p, f, f, None, f, f, f, f, ns - 1, f, ws, None, None,
+                                  None) == 3
+    assert lib.flce_backward_store(p, f, f, f, ns - 1, f, f, None, f, f, f, None, f, ws, None,
+                                   None, None) == 3
