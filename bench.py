@@ -30,8 +30,16 @@ V=128256, bf16, mean reduction, no bias, dloss = 1. Prints ONE JSON line
 * cpu_baseline / --impl reference: the CPU fp64 oracle timed on this host's
   cores on the same bounded token sample of the workload (a slow reference
   implementation, not a target).
-* --gpus N > 1 (torchrun): independent replicas, one per GPU ("replicas
-  only": the path is not sharded across GPUs); barrier + max over ranks.
+* --gpus N > 1 (torchrun): independent replicas, one per GPU, by default
+  (weak scaling: every rank runs the whole workload); barrier + max over
+  ranks. --parallel vocab splits the vocabulary instead (strong scaling):
+  rank r holds its contiguous shard of W's rows and runs the library's
+  vocabulary-shard calls, with the exchanges (a MAX and a SUM all-reduce of
+  per-token statistics, a SUM all-reduce of the fp32 partial dx) done by
+  NCCL all-reduces. Only the recompute mode exists for shards, and the shard
+  calls are not traced per kernel, so that line's roofline is the whole
+  step's. At N = 1 it runs the shard calls on one shard, the whole
+  vocabulary.
 """
 from __future__ import annotations
 
@@ -175,7 +183,7 @@ def workload_of(args):
     return wl
 
 
-def config_of(wl, ws: int) -> dict:
+def config_of(wl, ws: int, vocab_split: bool = False) -> dict:
     """The workload's description, the same in both arms' JSON lines."""
     opts = [wl.reduction, "bias" if wl.has_bias else "no bias"]
     if wl.label_smoothing:
@@ -189,7 +197,8 @@ def config_of(wl, ws: int) -> dict:
     opts.append(f"dloss={wl.dloss}")
     return {"workload": f"{wl.name}: N={wl.N} H={wl.H} V={wl.V} {wl.dtype}, " + ", ".join(opts),
             "N": wl.N, "H": wl.H, "V": wl.V, "dtype": wl.dtype,
-            "parallelism": "replicas" if ws > 1 else "single GPU",
+            "parallelism": (f"vocabulary split over {ws} GPU(s)" if vocab_split else
+                            "replicas" if ws > 1 else "single GPU"),
             "l2": "GPU arm: flushed (256 MiB write) before each timed step, outside the events"}
 
 
@@ -261,7 +270,7 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(wl, ws),
+        "config": config_of(wl, ws, args.parallel == "vocab"),
         "step": f"one oracle forward + backward over {rows} of the workload's {wl.N} tokens",
         "extrapolated_ms_per_full_step": per_step / rows * wl.N * 1e3,
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle_threads(),
@@ -277,19 +286,24 @@ def run_reference(args):
 
 class Problem:
     """Device inputs of one workload plus the buffers of one backward mode,
-    and one forward + backward step through the binding (C ABI)."""
+    and one forward + backward step through the binding (C ABI). With
+    `shard` = (start, end) only W's rows [start, end) are on the device and a
+    step runs the vocabulary-shard calls (vocab_parallel)."""
 
-    def __init__(self, torch, F, wl, dev, tdt, fkw, bkw):
+    def __init__(self, torch, F, wl, dev, tdt, fkw, bkw, shard=None):
         from linear_cross_entropy_gemm_gb300 import inputs as I
         self.torch, self.F, self.wl, self.dev = torch, F, wl, dev
         self.fkw, self.bkw = fkw, bkw
+        self.shard = shard
         inp = I.make_inputs(wl)
+        r0, r1 = shard if shard is not None else (0, wl.V)
         self.host_x = torch.from_numpy(inp.x.view(np.int16)).view(tdt).pin_memory()
         self.host_y = torch.from_numpy(inp.y).pin_memory()
         self.host_dl = torch.from_numpy(inp.dloss).pin_memory()
         self.x = self.host_x.to(dev)
-        self.W = torch.from_numpy(inp.W.view(np.int16)).view(tdt).to(dev)
-        self.b = None if inp.b is None else torch.from_numpy(inp.b.view(np.int16)).view(tdt).to(dev)
+        self.W = torch.from_numpy(inp.W[r0:r1].view(np.int16)).view(tdt).to(dev)
+        self.b = (None if inp.b is None else
+                  torch.from_numpy(inp.b[r0:r1].view(np.int16)).view(tdt).to(dev))
         self.y = self.host_y.to(dev)
         self.dloss = self.host_dl.to(dev)
         self.opts = options_of(wl)
@@ -299,6 +313,11 @@ class Problem:
     def allocate(self, mode):
         torch, F, wl = self.torch, self.F, self.wl
         N, H, V, dev = wl.N, wl.H, wl.V, self.dev
+        if self.shard is not None:
+            # The shard calls allocate their workspaces and outputs per call.
+            self.bufs = {"mode": mode, "fws": None, "bws": None, "state": None, "loss": None,
+                         "lse": None, "dx": None, "dW": None, "db": None}
+            return self.bufs
         bvb = self.bkw.get("bwd_vocab_block", 0)
         fp16 = self.tdt == torch.float16
         b = {"mode": mode}
@@ -329,6 +348,8 @@ class Problem:
 
     def scratch_bytes(self):
         b = self.bufs
+        if self.shard is not None:
+            return None  # allocated inside the shard calls: only the peak is known
         return sum(t.numel() for t in (b["fws"], b["bws"], b["state"]) if t is not None)
 
     def output_bytes(self):
@@ -341,6 +362,14 @@ class Problem:
         xb = self.x if xb is None else xb
         yb = self.y if yb is None else yb
         dlb = self.dloss if dlb is None else dlb
+        if self.shard is not None:
+            from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
+            sh = dict(vocab_start=self.shard[0], vocab_total=self.wl.V)
+            b["loss"], b["lse"] = VP.vocab_parallel_forward(xb, self.W, self.b, yb, **sh,
+                                                            **self.opts)
+            b["dx"], b["dW"], b["db"] = VP.vocab_parallel_backward(
+                dlb, b["lse"], xb, self.W, self.b, yb, **sh, **self.opts)
+            return
         st = {} if b["state"] is None else {("saved" if b["mode"] == "stored" else "kept"):
                                             b["state"]}
         F.flce_forward(xb, self.W, self.b, yb, workspace=b["fws"], out=(b["loss"], b["lse"]),
@@ -361,8 +390,8 @@ def end_to_end(torch, stream, prob, steps, barrier):
     host_in = (prob.host_x, prob.host_y, prob.host_dl)
     bufs = [(prob.x, prob.y, prob.dloss),
             (torch.empty_like(prob.x), torch.empty_like(prob.y), torch.empty_like(prob.dloss))]
-    loss = prob.bufs["loss"]
-    host_loss = torch.empty(loss.numel(), dtype=torch.float32).pin_memory()
+    host_loss = torch.empty(prob.wl.N if prob.wl.reduction == "none" else 1,
+                            dtype=torch.float32).pin_memory()
     copy_stream = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event(), torch.cuda.Event()]
     free = [torch.cuda.Event(), torch.cuda.Event()]
@@ -384,7 +413,7 @@ def end_to_end(torch, stream, prob, steps, barrier):
             xb, yb, dlb = bufs[i % 2]
             prob.step(xb=xb, yb=yb, dlb=dlb)
             free[i % 2].record(stream)
-            host_loss.copy_(loss, non_blocking=True)
+            host_loss.copy_(prob.bufs["loss"].reshape(-1), non_blocking=True)
 
     run(2)
     barrier()
@@ -455,7 +484,15 @@ def run_ours(args):
     N, H, V = wl.N, wl.H, wl.V
     fkw, bkw = {}, {"bwd_vocab_block": args.bwd_vocab_block}
     tune = None
-    prob = Problem(torch, F, wl, dev, tdt, fkw, bkw)
+    vocab_split = args.parallel == "vocab"
+    shard = None
+    if vocab_split:
+        from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
+        if args.autotune or V < 256 * ws:
+            raise SystemExit("--parallel vocab: no autotuning, and V must be >= 256 per rank")
+        args.mode, args.only_mode = "recompute", True  # the only mode of the shard calls
+        shard = VP.shard_range(V, ws, rank)
+    prob = Problem(torch, F, wl, dev, tdt, fkw, bkw, shard=shard)
     if args.autotune:
         res = tuning.autotune(prob.x, prob.W, prob.b, prob.y, dloss=prob.dloss, reps=3,
                               mode="kept" if args.mode == "kept" else "recompute", **prob.opts)
@@ -489,9 +526,10 @@ def run_ours(args):
         prob.step()
         barrier()
         free1 = torch.cuda.mem_get_info(dev)[0]
+        scratch = prob.scratch_bytes()
         mem = {"peak_extra_mib": (torch.cuda.max_memory_allocated(dev) - base) / 2**20,
-               "scratch_mib": prob.scratch_bytes() / 2**20,
-               "outputs_mib": prob.output_bytes() / 2**20,
+               "scratch_mib": None if scratch is None else scratch / 2**20,
+               "outputs_mib": None if scratch is None else prob.output_bytes() / 2**20,
                "device_free_drop_during_step_mib": (free0 - free1) / 2**20}
         clocks = ClockSampler(local) if mode == args.mode else None
         ms, per_kernel, launches, clk = timed_steps(torch, prob, args, stream, flush, barrier,
@@ -501,8 +539,9 @@ def run_ours(args):
         if mode == args.mode:
             e2e = end_to_end(torch, stream, prob, args.steps, barrier)
             e2e = (max_over_ranks(e2e[0], ws, dev), e2e[1], e2e[2])
+        loss_value = float(prob.bufs["loss"].double().sum())
         results[mode] = dict(ms=ms, per_kernel=per_kernel, launches=launches, clk=clk, mem=mem,
-                             e2e=e2e)
+                             e2e=e2e, loss=loss_value)
         prob.release()
 
     head = results[args.mode]
@@ -511,10 +550,25 @@ def run_ours(args):
     totals = {k: sum(v) for k, v in per_kernel.items()}
     kern = {k: {"launches_per_step": len(v) // steps_, "ms_per_step": sum(v) / steps_,
                 "share": sum(v) / sum(totals.values())} for k, v in sorted(per_kernel.items())}
-    dom = max(totals, key=totals.get)
-    dom_ms = totals[dom] / steps_
-    dom_flops = kernel_flops(dom, wl, bv_used, args.mode)
-    if dom_flops is not None:
+    dom = max(totals, key=totals.get) if totals else None
+    dom_ms = totals[dom] / steps_ if totals else None
+    dom_flops = kernel_flops(dom, wl, bv_used, args.mode) if totals else None
+    v_local = V if shard is None else shard[1] - shard[0]
+    if vocab_split:
+        # The shard calls are not traced per kernel: the roofline is the whole
+        # step's, one rank's 8 N H V_local flops over its step time.
+        achieved = 8.0 * N * H * v_local / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": "whole step (vocabulary shard)",
+                "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_sus"], "frac_of_burst_peak": achieved / pk["bf16"],
+                "peak_kind": f"bf16 sustained ({pk['src']})",
+                "algorithmic_flops_per_step": 8.0 * N * H * v_local, "traffic": None}
+        nblk = -(-v_local // tuning.library_default_block(N, v_local))
+        # forward GEMM + shard statistics, rescale, merge (+ finalize), prep,
+        # per block dlogits (+ db) + dW + dx, the fp32 -> 16-bit dx cast
+        head["launches"] = steps_ * (2 + 1 + (1 if wl.reduction == "none" else 2) + 1
+                                     + nblk * (3 + (1 if wl.has_bias else 0)) + 1)
+    elif dom_flops is not None:
         achieved = dom_flops / (dom_ms * 1e-3) / 1e12
         default_cfg = ((N, H, V) == (8192, 4096, 128256) and wl.dtype == "bf16"
                        and bv_used == tuning.library_default_block(N, V)
@@ -535,9 +589,12 @@ def run_ours(args):
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm"],
                 "unit": "GB/s", "frac": None, "traffic": None}
     flops_8 = 8.0 * N * H * V
-    executed = sum(kernel_flops(k, wl, bv_used, args.mode) or 0.0 for k in totals)
+    executed = (8.0 * N * H * V if vocab_split else
+                sum(kernel_flops(k, wl, bv_used, args.mode) or 0.0 for k in totals))
     tflops = flops_8 / (ms * 1e-3) / 1e12
-    value = ws * N / (ms * 1e-3)
+    # Replicas: every rank runs the whole workload. Vocabulary split: the
+    # ranks run one workload together.
+    value = (1 if vocab_split else ws) * N / (ms * 1e-3)
     e2e_ms, h2d, d2h = head["e2e"]
     other = {}
     for m, r in results.items():
@@ -545,7 +602,7 @@ def run_ours(args):
             continue
         other[m] = {"ms_per_step": r["ms"], "value": ws * N / (r["ms"] * 1e-3),
                     "unit": "tokens/s", "tflops_8nhv_equivalent": flops_8 / (r["ms"] * 1e-3) / 1e12,
-                    "memory": r["mem"],
+                    "memory": r["mem"], "loss": r["loss"],
                     "kernels": {k: {"launches_per_step": len(v) // steps_,
                                     "ms_per_step": sum(v) / steps_}
                                 for k, v in sorted(r["per_kernel"].items())}}
@@ -564,20 +621,22 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-        "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": (value / (ws * N / (PAGES_MS * 1e-3)) if wl.dtype == "bf16" and
-                        (N, H, V) == (8192, 4096, 128256) else None),
+        "higher_is_better": True, "scaling": "strong" if vocab_split else "weak",
+        "vs_baseline": (value / ((1 if vocab_split else ws) * N / (PAGES_MS * 1e-3))
+                        if wl.dtype == "bf16" and (N, H, V) == (8192, 4096, 128256) else None),
         "dtype": wl.dtype, "data": "synthetic",
-        "config": config_of(wl, ws),
+        "config": config_of(wl, ws, vocab_split),
         "impl_config": {"mode": args.mode, "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
-                        "gemm_form": forms_used},
+                        "gemm_form": forms_used,
+                        **({"vocab_shard": list(shard)} if vocab_split else {})},
+        "loss": head["loss"],
         "tflops_8nhv": tflops, "frac_bf16_peak_8nhv": tflops / pk["bf16_sus"],
         "frac_bf16_burst_8nhv": tflops / pk["bf16"],
         "tflops_executed": executed / (ms * 1e-3) / 1e12,
         "flops_executed_per_step": executed,
         "tflops_6nhv_useful": tflops * 0.75,
         "roofline": roof,
-        "kernels": kern,
+        "kernels": kern if not vocab_split else None,
         "gpu_launches": head["launches"],
         "memory": dict(head["mem"], **budget),
         "e2e": {"value": ws * N / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
@@ -608,6 +667,9 @@ def main():
     ap.add_argument("--mode", default="kept", choices=MODES,
                     help="backward mode of the timed step (the others are timed beside it)")
     ap.add_argument("--only-mode", action="store_true", help="time --mode only")
+    ap.add_argument("--parallel", default="replicas", choices=["replicas", "vocab"],
+                    help="ranks under torchrun: independent replicas (default) or one "
+                         "vocabulary split")
     ap.add_argument("--sample-rows", type=int, default=256,
                     help="tokens per oracle step (reference arm and cpu_baseline)")
     ap.add_argument("--oracle-threads", default=None,

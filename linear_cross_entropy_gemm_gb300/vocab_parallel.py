@@ -37,6 +37,20 @@ def _dist_allreduce(group) -> AllReduce:
     return f
 
 
+def shard_range(vocab_total: int, world: int, rank: int) -> tuple:
+    """The contiguous vocabulary rows [start, end) of rank `rank` when
+    `vocab_total` rows are split over `world` ranks: shard boundaries at
+    k * vocab_total / world rounded down to a multiple of 256 (the tile width),
+    so the shards differ by at most 256 rows, plus the ragged end the last one
+    takes. A vocabulary under 256 * world rows leaves some ranks empty."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError(f"shard_range: rank {rank} of {world}")
+
+    def bound(k):
+        return vocab_total if k == world else (k * vocab_total // world) // 256 * 256
+    return bound(rank), bound(rank + 1)
+
+
 def _shard_params(N, H, V_local, vocab_start, vocab_total, has_bias, fp16, opts):
     return params(N, H, V_local, has_bias=has_bias, vocab_start=vocab_start,
                   vocab_total=vocab_total, input_fp16=fp16, **opts)

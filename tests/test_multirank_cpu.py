@@ -160,3 +160,17 @@ def test_vocab_parallel_exchange_reports_a_lost_rank():
     assert all(p.exitcode is not None for p in procs), "a rank hung"
     assert procs[1].exitcode == 3
     assert procs[0].exitcode == _RAISED, f"survivor exit code {procs[0].exitcode}"
+
+
+@pytest.mark.parametrize("V,world", [(128256, 2), (128256, 8), (262144, 8), (1000, 3), (4096, 16)])
+def test_vocabulary_shard_plan(V, world):
+    # The bench's vocabulary split: contiguous shards that cover [0, V) in
+    # rank order, 256-aligned starts, sizes within 256 of each other (the last
+    # also takes the ragged end).
+    from linear_cross_entropy_gemm_gb300.vocab_parallel import shard_range
+    r = [shard_range(V, world, k) for k in range(world)]
+    assert r[0][0] == 0 and r[-1][1] == V
+    assert all(r[k][1] == r[k + 1][0] for k in range(world - 1))
+    assert all(a % 256 == 0 and b > a for a, b in r)
+    sizes = [b - a for a, b in r]
+    assert max(sizes) - min(sizes) <= 256 + V % 256
