@@ -614,9 +614,9 @@ def run_ours(args):
         "scratch_bound_mib": (N * bv_used * 2 + N * (bv_used // 32) * 4 + N * H * 4
                               + (4 * -(-N // 128) * bv_used * 4 if wl.has_bias else 0)
                               + N * -(-V // 256) * 12 + N * 32) / 2**20 + 1,
-        # The same with the stated reading of "one [N, BV] tile set plus the
-        # fp32 dW accumulator": the dL block and a [V, H] fp32 dW.
-        "north_star_budget_mib": (N * bv_used * 2 + V * H * 4) / 2**20,
+        # The method's memory budget, one [N, BV] block set plus an fp32
+        # [V, H] dW accumulator, with BV the backward vocabulary block.
+        "method_budget_mib": (N * bv_used * 2 + V * H * 4) / 2**20,
     }
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
