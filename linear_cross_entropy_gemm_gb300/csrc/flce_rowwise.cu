@@ -228,23 +228,47 @@ cudaError_t launch_prep(const PrepArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-__global__ void db_finalize_kernel(const float* __restrict__ part, int parts, int ld, int v0,
-                                   int Vb, void* db, int db_fp32, int fp16) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= Vb) return;
+// db[v0 + c] = sum over the partial rows p of part[p, c]. A block takes 32
+// columns (one coalesced 128-byte segment per partial row) and its 8 warps
+// split the partial rows: warp w sums rows w, w + 8, ... in order, with eight
+// independent loads in flight per thread; warp 0 then adds the 8 warp sums in
+// warp order. A fixed order throughout: deterministic.
+constexpr int kDbWarps = 8;
+__global__ void __launch_bounds__(32 * kDbWarps) db_finalize_kernel(
+    const float* __restrict__ part, int parts, int ld, int v0, int Vb, void* db, int db_fp32,
+    int fp16) {
+  __shared__ float s_sum[kDbWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int c = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int p = 0; p < parts; ++p) s += part[static_cast<size_t>(p) * ld + c];
+  if (c < Vb) {
+    int p = w;
+    for (; p + 7 * kDbWarps < parts; p += 8 * kDbWarps) {
+      float v[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) v[k] = __ldg(part + static_cast<size_t>(p + k * kDbWarps) * ld + c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s += v[k];
+    }
+    for (; p < parts; p += kDbWarps) s += __ldg(part + static_cast<size_t>(p) * ld + c);
+  }
+  s_sum[w][lane] = s;
+  __syncthreads();
+  if (w != 0 || c >= Vb) return;
+  float t = s_sum[0][lane];
+#pragma unroll
+  for (int k = 1; k < kDbWarps; ++k) t += s_sum[k][lane];
   if (db_fp32)
-    reinterpret_cast<float*>(db)[v0 + c] = s;
+    reinterpret_cast<float*>(db)[v0 + c] = t;
   else
     reinterpret_cast<uint16_t*>(db)[v0 + c] =
-        static_cast<uint16_t>(pack_16x2(s, 0.f, fp16 != 0) & 0xFFFFu);
+        static_cast<uint16_t>(pack_16x2(t, 0.f, fp16 != 0) & 0xFFFFu);
 }
 
 cudaError_t launch_db_finalize(const float* db_part, int parts, int ld, int v0, int Vb, void* db,
                                bool db_fp32, bool fp16, cudaStream_t st) {
-  db_finalize_kernel<<<(Vb + 255) / 256, 256, 0, st>>>(db_part, parts, ld, v0, Vb, db,
-                                                       db_fp32 ? 1 : 0, fp16 ? 1 : 0);
+  db_finalize_kernel<<<(Vb + 31) / 32, 32 * kDbWarps, 0, st>>>(db_part, parts, ld, v0, Vb, db,
+                                                              db_fp32 ? 1 : 0, fp16 ? 1 : 0);
   return cudaGetLastError();
 }
 
