@@ -233,6 +233,13 @@ struct FwdLseEpi {
     // once at the end.
     const float c2 = a.scale * kLog2e;
     const bool neg = c2 < 0.f;
+    // The second warp of a column-split pair reuses its staging buffer (the
+    // hand-off slots, and with KEEP the q boxes) only after its partner has
+    // read the previous hand-off.
+    if (sl.sub == 1 && sl.xcount > 0 &&
+        !mbar_wait(sl.xfree, static_cast<uint32_t>((sl.xcount - 1) & 1), sl.abort_flag,
+                   sl.dev_err))
+      return;
     float m = -INFINITY, d = 0.f, S = 0.f, ut = 0.f;
 #pragma unroll 1
     for (int c = sl.c_lo; c < sl.c_hi; ++c) {
@@ -311,6 +318,7 @@ struct FwdLseEpi {
     if (sl.sub == 0) {
       if (!mbar_wait(sl.xbar, sl.xph, sl.abort_flag, sl.dev_err)) return;
       const float4 o = sl.xchg[lane];
+      mbar_arrive(sl.xfree);  // the partner may reuse its staging buffer
       const float nm = fmaxf(m, o.x);
       // A half whose columns all lie past V has m = -inf and d = 0.
       d = nm == -INFINITY ? 0.f : d * fast_exp2(m - nm) + o.y * fast_exp2(o.x - nm);

@@ -62,13 +62,19 @@ struct GemmGeom {
 // epilogue warps) one half of them while a partner warp of the same TMEM lane
 // quarter takes the other; an epilogue whose row results span the sub-tile
 // then combines them: the second warp publishes its 32 rows' results in xchg
-// and arrives on xbar, the first waits (bounded) and merges.
+// (its own staging buffer) and arrives on xbar, the first waits (bounded),
+// reads them, arrives on xfree and merges. The second warp waits (bounded) on
+// xfree before it touches its staging buffer again in the next sub-tile it
+// hands off, so the hand-off never depends on how far ahead of its partner the
+// kernel's accumulator scheme lets it run.
 struct EpiSlice {
   int c_lo, c_hi;            // chunks [c_lo, c_hi) of the sub-tile's kBN / 32
   int sub;                   // -1: the whole sub-tile; 0 / 1: first / second half
-  uint64_t* xbar;            // sub >= 0: barrier of the pair (32 arrivals per phase)
+  uint64_t* xbar;            // sub >= 0: "published" barrier of the pair (32 arrivals)
+  uint64_t* xfree;           // sub >= 0: "read" barrier of the pair (32 arrivals)
   float4* xchg;              // sub >= 0: 32 slots, one per row, written by sub 1
   uint32_t xph;              // parity of xbar's phase for this sub-tile
+  int xcount;                // hand-offs completed before this sub-tile
   volatile int* abort_flag;  // the CTA's abort flag (for the bounded wait)
   int* dev_err;
 };
@@ -79,8 +85,10 @@ __device__ __forceinline__ EpiSlice whole_slice() {
   sl.c_hi = kBN / 32;
   sl.sub = -1;
   sl.xbar = nullptr;
+  sl.xfree = nullptr;
   sl.xchg = nullptr;
   sl.xph = 0;
+  sl.xcount = 0;
   sl.abort_flag = nullptr;
   sl.dev_err = nullptr;
   return sl;
@@ -522,6 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 //   tfull    (each CTA) : pair MMA commit after a tile's last K step
 //   tempty   (even CTA) : 2 x 32 kEW epilogue arrivals, one per epilogue thread
 //   xbar[8]  (each CTA) : kEW = 16 only; a column-split warp pair's hand-off
+//   xfree[8] (each CTA) : kEW = 16 only; the hand-off has been read
 constexpr int kWideStages = 4;
 constexpr int kWideBHalfBytes = (kBN / 2) * kBK * 2;           // 16 KiB
 constexpr int kWideBStageBytes = 2 * kWideBHalfBytes;          // 32 KiB
@@ -556,6 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide_threads(kEW), 1
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   uint64_t* xbar = done_bar + 2;  // [2 halves x 4 lane quarters], kEW = 16
+  uint64_t* xfree = xbar + 8;     // [2 halves x 4 lane quarters], kEW = 16
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -573,7 +583,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide_threads(kEW), 1
     mbar_init(tempty, 2 * 32 * kEW);
     mbar_init(done_bar, 1);
     if constexpr (kEW == 16)
-      for (int i = 0; i < 8; ++i) mbar_init(&xbar[i], 32);
+      for (int i = 0; i < 8; ++i) {
+        mbar_init(&xbar[i], 32);
+        mbar_init(&xfree[i], 32);
+      }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -724,8 +737,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide_threads(kEW), 1
     sl.c_lo = (sl.sub < 0 ? 0 : sl.sub) * kChunks;
     sl.c_hi = sl.c_lo + kChunks;
     sl.xbar = &xbar[half * 4 + quad];
+    sl.xfree = &xfree[half * 4 + quad];
     sl.xchg = reinterpret_cast<float4*>(sl.sub == 0 ? my_stage + 4 * kWarpStage : my_stage);
     sl.xph = 0;
+    sl.xcount = 0;
     sl.abort_flag = abort_flag;
     sl.dev_err = dev_err;
     const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
@@ -743,6 +758,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide_threads(kEW), 1
         Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr,
                   my_stage, sl);
         sl.xph ^= 1;
+        ++sl.xcount;
       }
       tc_fence_before();
       mbar_arrive_cluster(tempty0);
