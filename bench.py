@@ -36,9 +36,10 @@ V=128256, bf16, mean reduction, no bias, dloss = 1. Prints ONE JSON line
   rank r holds its contiguous shard of W's rows and runs the library's
   vocabulary-shard calls, with the exchanges (a MAX and a SUM all-reduce of
   per-token statistics, a SUM all-reduce of the fp32 partial dx) done by
-  NCCL all-reduces. Only the recompute mode exists for shards, and the shard
-  calls are not traced per kernel, so that line's roofline is the whole
-  step's. At N = 1 it runs the shard calls on one shard, the whole
+  NCCL all-reduces. Each shard keeps its own first block in the kept mode
+  (recompute with --mode recompute; no stored mode for shards), and the
+  shard calls are not traced per kernel, so that line's roofline is the
+  whole step's. At N = 1 it runs the shard calls on one shard, the whole
   vocabulary.
 """
 from __future__ import annotations
@@ -315,8 +316,16 @@ class Problem:
         torch, F, wl = self.torch, self.F, self.wl
         N, H, V, dev = wl.N, wl.H, wl.V, self.dev
         if self.shard is not None:
-            # The shard calls allocate their workspaces and outputs per call.
-            self.bufs = {"mode": mode, "fws": None, "bws": None, "state": None, "loss": None,
+            # The shard calls allocate their workspaces and outputs per call;
+            # the kept block is the caller's.
+            from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
+            kept = None
+            if mode == "kept":
+                kept = torch.empty(VP.kept_size(
+                    N, H, self.shard[1] - self.shard[0], vocab_start=self.shard[0],
+                    vocab_total=V, bwd_vocab_block=self.bkw.get("bwd_vocab_block", 0),
+                    input_fp16=self.tdt == torch.float16), dtype=torch.uint8, device=dev)
+            self.bufs = {"mode": mode, "fws": None, "bws": None, "state": kept, "loss": None,
                          "lse": None, "dx": None, "dW": None, "db": None}
             return self.bufs
         bvb = self.bkw.get("bwd_vocab_block", 0)
@@ -365,7 +374,8 @@ class Problem:
         dlb = self.dloss if dlb is None else dlb
         if self.shard is not None:
             from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
-            sh = dict(vocab_start=self.shard[0], vocab_total=self.wl.V)
+            sh = dict(vocab_start=self.shard[0], vocab_total=self.wl.V, kept=b["state"],
+                      bwd_vocab_block=self.bkw.get("bwd_vocab_block", 0))
             b["loss"], b["lse"] = VP.vocab_parallel_forward(xb, self.W, self.b, yb, **sh,
                                                             **self.opts)
             b["dx"], b["dW"], b["db"] = VP.vocab_parallel_backward(
@@ -489,9 +499,10 @@ def run_ours(args):
     shard = None
     if vocab_split:
         from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
-        if args.autotune or V < 256 * ws:
-            raise SystemExit("--parallel vocab: no autotuning, and V must be >= 256 per rank")
-        args.mode, args.only_mode = "recompute", True  # the only mode of the shard calls
+        if args.autotune or V < 256 * ws or args.mode == "stored":
+            raise SystemExit("--parallel vocab: kept or recompute mode, no autotuning, and "
+                             "V >= 256 per rank")
+        args.only_mode = True
         shard = VP.shard_range(V, ws, rank)
     prob = Problem(torch, F, wl, dev, tdt, fkw, bkw, shard=shard)
     if args.autotune:
@@ -557,13 +568,16 @@ def run_ours(args):
     v_local = V if shard is None else shard[1] - shard[0]
     if vocab_split:
         # The shard calls are not traced per kernel: the roofline is the whole
-        # step's, one rank's 8 N H V_local flops over its step time.
-        achieved = 8.0 * N * H * v_local / (ms * 1e-3) / 1e12
+        # step's, one rank's executed flops over its step time.
+        kept_cols = min(tuning.library_default_block(N, v_local) if not bvb else bvb, v_local)
+        step_flops = 8.0 * N * H * v_local - (2.0 * N * H * kept_cols if args.mode == "kept"
+                                               else 0)
+        achieved = step_flops / (ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "kernel": "whole step (vocabulary shard)",
                 "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
                 "frac": achieved / pk["bf16_sus"], "frac_of_burst_peak": achieved / pk["bf16"],
                 "peak_kind": f"bf16 sustained ({pk['src']})",
-                "algorithmic_flops_per_step": 8.0 * N * H * v_local, "traffic": None}
+                "algorithmic_flops_per_step": step_flops, "traffic": None}
         nblk = -(-v_local // tuning.library_default_block(N, v_local))
         # forward GEMM + shard statistics, rescale, merge (+ finalize), prep,
         # per block dlogits (+ db) + dW + dx, the fp32 -> 16-bit dx cast
@@ -590,8 +604,11 @@ def run_ours(args):
         roof = {"bound": "hbm", "kernel": dom, "achieved": None, "peak": pk["hbm"],
                 "unit": "GB/s", "frac": None, "traffic": None}
     flops_8 = 8.0 * N * H * V
-    executed = (8.0 * N * H * V if vocab_split else
-                sum(kernel_flops(k, wl, bv_used, args.mode) or 0.0 for k in totals))
+    if vocab_split:
+        kept_cols = min(tuning.library_default_block(N, v_local) if not bvb else bvb, v_local)
+        executed = 8.0 * N * H * v_local - (2.0 * N * H * kept_cols if args.mode == "kept" else 0)
+    else:
+        executed = sum(kernel_flops(k, wl, bv_used, args.mode) or 0.0 for k in totals)
     tflops = flops_8 / (ms * 1e-3) / 1e12
     # Replicas: every rank runs the whole workload. Vocabulary split: the
     # ranks run one workload together.

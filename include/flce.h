@@ -209,8 +209,8 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
  * half of the recompute, an eighth of the step's flops.
  * Both calls take the same p (the kept layout depends on N, V and BVc); the
  * backward consumes the kept state (it holds dL afterwards), and the buffer
- * must be left untouched between the two calls. Plain (whole-vocabulary)
- * calls only; trace may be NULL.
+ * must be left untouched between the two calls. The vocabulary-shard calls
+ * have kept-block forms too (below). trace may be NULL.
  */
 size_t flce_kept_size(const flce_params_t* p);
 flce_status_t flce_forward_keep(const flce_params_t* p, const void* x, const void* W,
@@ -285,6 +285,23 @@ flce_status_t flce_backward_shard(const flce_params_t* p, const float* dloss, co
                                   size_t workspace_bytes, int32_t* dev_err, void* stream);
 flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_fp16,
                             void* stream);
+
+/* Steps 1 and 6 with the kept block: the shard's forward also keeps the
+ * probabilities of its own first backward vocabulary block (its rows
+ * [vocab_start, vocab_start + BVc), BVc per p as in flce_forward_keep), and
+ * the shard's backward converts them in place instead of recomputing them.
+ * kept: flce_kept_size(p) bytes for the shard's p, 16-byte aligned, consumed
+ * by the backward; the backward's workspace is flce_workspace_size(p, 2). */
+flce_status_t flce_forward_shard_keep(const flce_params_t* p, const void* x, const void* W,
+                                      const void* b, const int64_t* y, float* stats, void* kept,
+                                      size_t kept_bytes, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_err, void* stream);
+flce_status_t flce_backward_shard_keep(const flce_params_t* p, const float* dloss,
+                                       const float* lse, void* kept, size_t kept_bytes,
+                                       const void* x, const void* W, const void* b,
+                                       const int64_t* y, float* dx_partial, void* dW, void* db,
+                                       void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                       void* stream);
 
 /*
  * Forward without a workspace argument, for callers that cannot allocate

@@ -110,6 +110,11 @@ def load() -> ctypes.CDLL:
     lib.flce_backward_keep.restype = ctypes.c_int
     lib.flce_forward_shard.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp, vp]
     lib.flce_forward_shard.restype = ctypes.c_int
+    lib.flce_forward_shard_keep.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp, sz, vp, vp]
+    lib.flce_forward_shard_keep.restype = ctypes.c_int
+    lib.flce_backward_shard_keep.argtypes = [P, vp, vp, vp, sz, vp, vp, vp, vp, vp, vp, vp, vp,
+                                             sz, vp, vp]
+    lib.flce_backward_shard_keep.restype = ctypes.c_int
     lib.flce_shard_rescale.argtypes = [P, vp, vp, vp]
     lib.flce_shard_rescale.restype = ctypes.c_int
     lib.flce_loss_from_stats.argtypes = [P, vp, vp, vp, vp, vp, sz, vp, vp]

@@ -427,7 +427,7 @@ size_t flce_saved_size(const flce_params_t* p) {
 }
 
 size_t flce_kept_size(const flce_params_t* p) {
-  if (check_params(p) != FLCE_OK || p->N == 0 || !whole_vocab(p)) return 0;
+  if (check_params(p) != FLCE_OK || p->N == 0) return 0;
   Kept k{};
   return carve_kept(p, nullptr, &k);
 }
@@ -473,7 +473,6 @@ static flce_status_t forward_impl(const char* name, const flce_params_t* p, cons
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   Kept kp{};  // filled by carve_kept when `kept` is given
   if (kept) {
-    if (shard_stats) return FLCE_ERR_INVALID_ARG;
     if (kept_bytes < carve_kept(p, nullptr, &kp)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(kept)) return FLCE_ERR_ALIGNMENT;
   }
@@ -644,7 +643,6 @@ static flce_status_t backward_impl(const char* name, const flce_params_t* p, con
   if (workspace_bytes < need) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   Kept kp{};  // filled by carve_kept when `kept` is given
   if (kept) {
-    if (shard) return FLCE_ERR_INVALID_ARG;
     if (kept_bytes < carve_kept(p, nullptr, &kp)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
     if (!aligned16(kept)) return FLCE_ERR_ALIGNMENT;
     carve_kept(p, kept, &kp);
@@ -810,6 +808,16 @@ flce_status_t flce_forward_shard(const flce_params_t* p, const void* x, const vo
                       workspace_bytes, dev_err, stream, nullptr, stats);
 }
 
+flce_status_t flce_forward_shard_keep(const flce_params_t* p, const void* x, const void* W,
+                                      const void* b, const int64_t* y, float* stats, void* kept,
+                                      size_t kept_bytes, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_err, void* stream) {
+  if (!p) return FLCE_ERR_INVALID_ARG;
+  if ((!stats || !kept) && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return forward_impl("flce_forward_shard_keep", p, x, W, b, y, nullptr, nullptr, workspace,
+                      workspace_bytes, dev_err, stream, nullptr, stats, kept, kept_bytes);
+}
+
 flce_status_t flce_shard_rescale(const flce_params_t* p, float* stats, const float* global_max,
                                  void* stream) {
   flce_status_t st = check_params(p);
@@ -872,6 +880,19 @@ flce_status_t flce_backward_shard(const flce_params_t* p, const float* dloss, co
                                   size_t workspace_bytes, int32_t* dev_err, void* stream) {
   return backward_impl("flce_backward_shard", p, dloss, lse, x, W, b, y, dx_partial, dW, db,
                        workspace, workspace_bytes, dev_err, stream, nullptr, true);
+}
+
+flce_status_t flce_backward_shard_keep(const flce_params_t* p, const float* dloss,
+                                       const float* lse, void* kept, size_t kept_bytes,
+                                       const void* x, const void* W, const void* b,
+                                       const int64_t* y, float* dx_partial, void* dW, void* db,
+                                       void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                       void* stream) {
+  if (!p) return FLCE_ERR_INVALID_ARG;
+  if (!kept && p->N > 0) return FLCE_ERR_INVALID_ARG;
+  return backward_impl("flce_backward_shard_keep", p, dloss, lse, x, W, b, y, dx_partial, dW, db,
+                       workspace, workspace_bytes, dev_err, stream, nullptr, true, kept,
+                       kept_bytes);
 }
 
 flce_status_t flce_cast_f32(const float* src, void* dst, int64_t n, int32_t dst_fp16,

@@ -14,6 +14,12 @@ The collectives are torch.distributed all-reduces on ``group`` (skipped when
 there is a single rank); ``allreduce`` may replace them (a function
 ``allreduce(tensor, op)`` with op "max" or "sum", reducing in place).
 All arithmetic runs in the library's CUDA kernels.
+
+With ``kept`` (a uint8 CUDA tensor of ``kept_size`` bytes, the same on the
+forward and the backward of a shard) the shard's forward also keeps the
+probabilities of its own first backward vocabulary block, and its backward
+converts them instead of recomputing that block (the kept-block mode of the
+whole-vocabulary calls, per shard).
 """
 from __future__ import annotations
 
@@ -51,22 +57,48 @@ def shard_range(vocab_total: int, world: int, rank: int) -> tuple:
     return bound(rank), bound(rank + 1)
 
 
-def _shard_params(N, H, V_local, vocab_start, vocab_total, has_bias, fp16, opts):
+def _shard_params(N, H, V_local, vocab_start, vocab_total, has_bias, fp16, opts,
+                  bwd_vocab_block=0):
     return params(N, H, V_local, has_bias=has_bias, vocab_start=vocab_start,
-                  vocab_total=vocab_total, input_fp16=fp16, **opts)
+                  vocab_total=vocab_total, input_fp16=fp16, bwd_vocab_block=bwd_vocab_block,
+                  **opts)
 
 
-def forward_shard(x, W, b, y, *, vocab_start, vocab_total, stream=None, **opts) -> torch.Tensor:
-    """This shard's per-token statistics, a [4, N] fp32 tensor (m, d, z_y, sum z)."""
+def kept_size(N, H, V_local, *, vocab_start, vocab_total, bwd_vocab_block=0,
+              input_fp16=False) -> int:
+    """Bytes of a shard's kept state (flce_kept_size for the shard's rows)."""
+    p = params(N, H, V_local, vocab_start=vocab_start, vocab_total=vocab_total,
+               bwd_vocab_block=bwd_vocab_block, input_fp16=input_fp16)
+    return int(_lib.load().flce_kept_size(p))
+
+
+def _check_kept(kept, lib, p):
+    if kept.dtype != torch.uint8 or not kept.is_cuda or not kept.is_contiguous():
+        raise TypeError("flce: kept must be a contiguous uint8 CUDA tensor")
+    if kept.numel() < lib.flce_kept_size(p):
+        raise ValueError("flce: kept is smaller than the shard's flce_kept_size()")
+
+
+def forward_shard(x, W, b, y, *, vocab_start, vocab_total, stream=None, kept=None,
+                  bwd_vocab_block=0, **opts) -> torch.Tensor:
+    """This shard's per-token statistics, a [4, N] fp32 tensor (m, d, z_y, sum z);
+    with ``kept``, also the shard's kept block (for backward_shard(kept=))."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
     p = _shard_params(N, H, W.shape[0], vocab_start, vocab_total, b is not None,
-                      x.dtype == torch.float16, opts)
+                      x.dtype == torch.float16, opts, bwd_vocab_block)
     stats = torch.empty(4, N, dtype=torch.float32, device=x.device)
     ws = torch.empty(max(lib.flce_workspace_size(p, 0), 1), dtype=torch.uint8, device=x.device)
-    st = lib.flce_forward_shard(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(stats), _ptr(ws),
-                                ws.numel(), _ptr(device_error_word(x.device)), _stream(stream))
+    if kept is not None:
+        _check_kept(kept, lib, p)
+        st = lib.flce_forward_shard_keep(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(stats),
+                                         _ptr(kept), kept.numel(), _ptr(ws), ws.numel(),
+                                         _ptr(device_error_word(x.device)), _stream(stream))
+    else:
+        st = lib.flce_forward_shard(p, _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(stats),
+                                    _ptr(ws), ws.numel(), _ptr(device_error_word(x.device)),
+                                    _stream(stream))
     if st != _lib.FLCE_OK:
         raise FlceError(st, "flce_forward_shard")
     return stats
@@ -111,8 +143,11 @@ def loss_from_stats(stats, y, *, vocab_total, H, stream=None, **opts):
 
 
 def backward_shard(dloss, lse, x, W, b, y, *, vocab_start, vocab_total, stream=None,
-                   dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0, **opts):
-    """This shard's dW rows, db, and its fp32 partial dx [N, H]."""
+                   dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0,
+                   kept=None, **opts):
+    """This shard's dW rows, db, and its fp32 partial dx [N, H]; with ``kept``
+    (filled by forward_shard(kept=) with the same bwd_vocab_block), the kept
+    block's dlogits come from the kept probabilities."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
@@ -125,10 +160,18 @@ def backward_shard(dloss, lse, x, W, b, y, *, vocab_start, vocab_total, stream=N
     dx = torch.empty(N, H, dtype=torch.float32, device=dev)
     dW = torch.empty(V, H, dtype=dW_dtype, device=dev)
     db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
-    ws = torch.empty(max(lib.flce_workspace_size(p, 1), 1), dtype=torch.uint8, device=dev)
-    st = lib.flce_backward_shard(p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b), _ptr(y),
-                                 _ptr(dx), _ptr(dW), _ptr(db), _ptr(ws), ws.numel(),
-                                 _ptr(device_error_word(dev)), _stream(stream))
+    ws = torch.empty(max(lib.flce_workspace_size(p, 2 if kept is not None else 1), 1),
+                     dtype=torch.uint8, device=dev)
+    if kept is not None:
+        _check_kept(kept, lib, p)
+        st = lib.flce_backward_shard_keep(p, _ptr(dloss), _ptr(lse), _ptr(kept), kept.numel(),
+                                          _ptr(x), _ptr(W), _ptr(b), _ptr(y), _ptr(dx), _ptr(dW),
+                                          _ptr(db), _ptr(ws), ws.numel(),
+                                          _ptr(device_error_word(dev)), _stream(stream))
+    else:
+        st = lib.flce_backward_shard(p, _ptr(dloss), _ptr(lse), _ptr(x), _ptr(W), _ptr(b),
+                                     _ptr(y), _ptr(dx), _ptr(dW), _ptr(db), _ptr(ws), ws.numel(),
+                                     _ptr(device_error_word(dev)), _stream(stream))
     if st != _lib.FLCE_OK:
         raise FlceError(st, "flce_backward_shard")
     return dx, dW, db
@@ -145,11 +188,14 @@ def cast16(src: torch.Tensor, dtype=torch.bfloat16, stream=None) -> torch.Tensor
 
 
 def vocab_parallel_forward(x, W_local, b_local, y, *, vocab_start: int, vocab_total: int,
-                           group=None, allreduce: Optional[AllReduce] = None, **opts):
-    """Whole-vocabulary loss and lse on every rank from its vocabulary shard."""
+                           group=None, allreduce: Optional[AllReduce] = None, kept=None,
+                           bwd_vocab_block: int = 0, **opts):
+    """Whole-vocabulary loss and lse on every rank from its vocabulary shard
+    (``kept``: this shard's kept block, for vocab_parallel_backward)."""
     ar = allreduce or _dist_allreduce(group)
     stats = forward_shard(x, W_local, b_local, y, vocab_start=vocab_start,
-                          vocab_total=vocab_total, **opts)
+                          vocab_total=vocab_total, kept=kept, bwd_vocab_block=bwd_vocab_block,
+                          **opts)
     merge_stats(stats, ar)
     return loss_from_stats(stats, y, vocab_total=vocab_total, H=x.shape[1], **opts)
 
@@ -157,7 +203,8 @@ def vocab_parallel_forward(x, W_local, b_local, y, *, vocab_start: int, vocab_to
 def vocab_parallel_backward(dloss, lse, x, W_local, b_local, y, *, vocab_start: int,
                             vocab_total: int, group=None, allreduce: Optional[AllReduce] = None,
                             **opts):
-    """bf16 dx (summed over shards in fp32), this shard's dW rows and db."""
+    """bf16 dx (summed over shards in fp32), this shard's dW rows and db
+    (``kept`` and ``bwd_vocab_block`` as given to vocab_parallel_forward)."""
     ar = allreduce or _dist_allreduce(group)
     dx32, dW, db = backward_shard(dloss, lse, x, W_local, b_local, y, vocab_start=vocab_start,
                                   vocab_total=vocab_total, **opts)

@@ -152,8 +152,10 @@ def test_kept_and_stored_sizes(lib):
     assert lib.flce_workspace_size(p, 3) < lib.flce_workspace_size(p, 2)
     assert lib.flce_workspace_size(p, 4) == 0
     assert lib.flce_kept_size(_lib.params(0, 64, 10)) == 0
-    # a vocabulary shard has no kept or stored mode
-    assert lib.flce_kept_size(_lib.params(4, 64, 10, vocab_start=10, vocab_total=40)) == 0
+    # a vocabulary shard keeps its own first block; it has no stored mode
+    shard = _lib.params(4, 64, 10, vocab_start=10, vocab_total=40)
+    assert lib.flce_kept_size(shard) == lib.flce_kept_size(_lib.params(4, 64, 10)) > 0
+    assert lib.flce_saved_size(shard) == 0
 
 
 def test_kept_entry_points_reject_bad_arguments_on_host(lib):

@@ -68,11 +68,12 @@ def test_gpu_arm_line():
 def test_gpu_vocab_split_line_matches_the_replica_loss():
     # At one GPU the vocabulary split runs the shard calls on a single shard
     # (the whole vocabulary); its loss equals the plain path's.
-    common = ["--steps", "3", "--warmup", "3", "--shape", "1024,256,8192", "--no-cpu-baseline",
-              "--mode", "recompute", "--only-mode"]
-    plain = _run(common)
-    split = _run(common + ["--parallel", "vocab"])
-    assert split["scaling"] == "strong" and split["impl_config"]["vocab_shard"] == [0, 8192]
-    assert split["config"]["parallelism"].startswith("vocabulary split")
-    assert split["roofline"]["bound"] == "tensor" and split["gpu_launches"] > 0
-    assert abs(split["loss"] - plain["loss"]) <= 1e-6 * abs(plain["loss"])
+    for mode in ("recompute", "kept"):
+        common = ["--steps", "3", "--warmup", "3", "--shape", "1024,256,8192",
+                  "--no-cpu-baseline", "--mode", mode, "--only-mode"]
+        plain = _run(common)
+        split = _run(common + ["--parallel", "vocab"])
+        assert split["scaling"] == "strong" and split["impl_config"]["vocab_shard"] == [0, 8192]
+        assert split["config"]["parallelism"].startswith("vocabulary split")
+        assert split["roofline"]["bound"] == "tensor" and split["gpu_launches"] > 0
+        assert abs(split["loss"] - plain["loss"]) <= 1e-6 * abs(plain["loss"])

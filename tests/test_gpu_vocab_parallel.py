@@ -25,9 +25,10 @@ def _sim_allreduce(tensors):
     return run
 
 
+@pytest.mark.parametrize("mode", ["recompute", "kept"])
 @pytest.mark.parametrize("form", ["default", "single", "wide"])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-def test_uneven_shards_match_whole_vocabulary(reduction, form, monkeypatch):
+def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, monkeypatch):
     # The shard calls take no gemm_form of their own: the environment override
     # selects the kernel form for every call of the test (shard offsets in the
     # wide and single-CTA kernels as well as the default pairs).
@@ -43,9 +44,18 @@ def test_uneven_shards_match_whole_vocabulary(reduction, form, monkeypatch):
     cuts = [0, 1000, 2256, 3001]
     shards = [(a, b - a) for a, b in zip(cuts[:-1], cuts[1:])]
 
+    # Kept mode: each shard keeps its own first 512-column block (the second
+    # and third shards are wider than one block, the first is exactly 1000).
+    bvb = 512
+    kept = [VP.kept_size(wl.N, wl.H, n, vocab_start=a, vocab_total=wl.V, bwd_vocab_block=bvb)
+            for a, n in shards] if mode == "kept" else [0] * len(shards)
+    kept = [torch.empty(k, dtype=torch.uint8, device=prob.dev) if k else None for k in kept]
+
     # forward: local stats, MAX of m, rescale, SUM of (d, z_y, sum z)
     stats = [VP.forward_shard(prob.x, prob.W[a:a + n].contiguous(), prob.b[a:a + n].contiguous(),
-                              prob.y, vocab_start=a, vocab_total=wl.V, **opts) for a, n in shards]
+                              prob.y, vocab_start=a, vocab_total=wl.V, kept=k,
+                              bwd_vocab_block=bvb, **opts)
+             for (a, n), k in zip(shards, kept)]
     gmax = [s[0].clone() for s in stats]
     _sim_allreduce(gmax)("max")
     for s, m in zip(stats, gmax):
@@ -56,7 +66,8 @@ def test_uneven_shards_match_whole_vocabulary(reduction, form, monkeypatch):
     # backward: per-shard dW rows, db, fp32 dx partials summed then cast once
     parts = [VP.backward_shard(prob.dloss, lse, prob.x, prob.W[a:a + n].contiguous(),
                                prob.b[a:a + n].contiguous(), prob.y, vocab_start=a,
-                               vocab_total=wl.V, **opts) for a, n in shards]
+                               vocab_total=wl.V, kept=k, bwd_vocab_block=bvb, **opts)
+             for (a, n), k in zip(shards, kept)]
     dx32 = [p[0] for p in parts]
     _sim_allreduce(dx32)("sum")
     dx = VP.cast16(dx32[0])
