@@ -3,16 +3,22 @@
 //
 // Forward  (DeepSpeed PR #8792 "What": forward keeps per-token softmax
 //           statistics only):
-//   fwd_lse GEMM  x W^T tile by tile -> (m, d[, sum z]) partials + z_y
+//   fwd_lse GEMM  x W^T tile by tile -> (m, d[, sum z]) partials + z_y; in the
+//                 kept-block mode also the first backward block's fp16
+//                 probabilities and their 32-column running maxima
 //   merge         partials -> lse, per-token loss, reduction
 // Backward (same page: logits recomputed one vocabulary block at a time, so
 //           each dW block is one GEMM over all tokens):
 //   prep          per-token coefficients from dloss, lse, y
 //   per vocab block [v0, v0 + Vb):
-//     dlogits GEMM  recompute x W_blk^T -> dL_blk = s dz (bf16) + db partials
+//     dlogits GEMM  recompute x W_blk^T -> dL_blk = s dz (bf16) + db partials,
+//                   or, for the kept block, the in-place conversion of its
+//                   kept probabilities
 //     dW GEMM       dW[v0:v0+Vb] = dL_blk^T x            (K = all tokens)
 //     dx GEMM       dx (+)= dL_blk W_blk                  (fp32 across blocks)
 //     db finalize   (with a bias)
+// The stored-probability mode is the kept-block mode with one block over the
+// whole vocabulary.
 #include <algorithm>
 #include <cstdint>
 #include <cstdlib>
