@@ -222,13 +222,14 @@ def test_autograd_module_matches_c_abi(mode):
 _cache = {}
 
 
-def _sampled(name):
+def _sampled(name, wl=None, modes=MODES):
     """GPU outputs plus the oracle on every token's statistics, 256 sampled
-    dx rows and 256 sampled dW / db rows, for one full-size problem."""
+    dx rows and 256 sampled dW / db rows, for one full-size problem (a named
+    workload, or `wl` under that name) in the given backward modes."""
     if name in _cache:
         return _cache[name]
     _cache.clear()
-    wl = I.WORKLOADS[name]
+    wl = I.WORKLOADS[name] if wl is None else wl
     inp = I.make_inputs(wl)
     prob = DeviceProblem(inp)
     opts = opts_of(wl)
@@ -255,7 +256,7 @@ def _sampled(name):
     rdx = O.dx_rows(rows, dl, x64, W64, b64, inp.y, **opts)
     rdW, rdb = O.dW_db_rows(vrows, lse, dl, x64, W64, b64, inp.y, **opts)
     got = {}
-    for mode in MODES:
+    for mode in modes:
         out = prob.run(mode=mode)
         assert out["err"] == 0, f"device error word {out['err']}"
         got[mode] = dict(loss=to_np(out["loss"]), lse=to_np(out["lse"]),
@@ -280,6 +281,22 @@ def test_full_size_sampled(name, mode):
     assert_grad_close(g["dW"], ref["dW"], f"{name} dW (sampled vocab rows)")
     if wl.has_bias:
         assert_grad_close(g["db"], ref["db"], f"{name} db (sampled)")
+
+
+@pytest.mark.parametrize("mode", ["kept", "recompute"])
+def test_full_size_sampled_fp16_llama3_head(mode):
+    # The headline shape with fp16 operands (the loss-scale-safe dL path). dx
+    # is written in fp16: unscaled, the mean over 8192 tokens puts it near
+    # 2e-6, in fp16's subnormals; as in fp16 training a loss scale (1024)
+    # keeps it in range.
+    wl = I.WORKLOADS["llama3_head"].with_(name="llama3_head_fp16", dtype="fp16",
+                                          dloss_scale=1024.0)
+    r = _sampled("llama3_head_fp16", wl, modes=["kept", "recompute"])
+    g, ref = r["got"][mode], r["ref"]
+    assert_loss_close(g["loss"], ref["loss"], "fp16 llama3_head loss")
+    assert_loss_close(g["lse"], ref["lse"], "fp16 llama3_head lse (all tokens)")
+    assert_grad_close(g["dx"], ref["dx"], "fp16 llama3_head dx (sampled rows)")
+    assert_grad_close(g["dW"], ref["dW"], "fp16 llama3_head dW (sampled vocab rows)")
 
 
 def test_bounded_wait_times_out_with_a_status_and_the_context_survives():
