@@ -1,5 +1,5 @@
 """flce_forward + flce_backward captured into one CUDA graph, in the
-recompute and the kept-block modes: the calls make no host synchronisation
+recompute, kept-block and stored modes: the calls make no host synchronisation
 or allocation of their own (the caller passes the workspace, the kept
 buffer and the outputs), so a replay runs the same kernels on the captured
 buffers. The library is run-to-run deterministic, so a replay must equal an
@@ -21,7 +21,7 @@ def _problem(seed):
     return wl, inp
 
 
-@pytest.mark.parametrize("mode", ["recompute", "kept"])
+@pytest.mark.parametrize("mode", ["recompute", "kept", "stored"])
 @pytest.mark.parametrize("form", ["single", "pair", "wide"])
 def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form, mode):
     wl, inp = _problem(41)
@@ -35,12 +35,16 @@ def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form, mode):
     N, H, V = wl.N, wl.H, wl.V
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", has_bias=True, **opts),
                       dtype=torch.uint8, device=dev)
-    keep = mode == "kept"
-    bws = torch.empty(F.flce_workspace_size(N, H, V, "backward_keep" if keep else "backward",
-                                            has_bias=True, bwd_vocab_block=1024, **opts),
-                      dtype=torch.uint8, device=dev)
-    kept = (torch.empty(F.flce_kept_size(N, H, V, bwd_vocab_block=1024), dtype=torch.uint8,
-                        device=dev) if keep else None)
+    kind = {"kept": "backward_keep", "stored": "backward_store"}.get(mode, "backward")
+    bws = torch.empty(F.flce_workspace_size(N, H, V, kind, has_bias=True, bwd_vocab_block=1024,
+                                            **opts), dtype=torch.uint8, device=dev)
+    state = {}
+    if mode == "kept":
+        state = dict(kept=torch.empty(F.flce_kept_size(N, H, V, bwd_vocab_block=1024),
+                                      dtype=torch.uint8, device=dev))
+    elif mode == "stored":
+        state = dict(saved=torch.empty(F.flce_saved_size(N, H, V), dtype=torch.uint8,
+                                       device=dev))
     loss = torch.empty(1, dtype=torch.float32, device=dev)
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     dx = torch.empty(N, H, dtype=torch.bfloat16, device=dev)
@@ -48,10 +52,10 @@ def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form, mode):
     db = torch.empty(V, dtype=torch.float32, device=dev)
 
     def step():
-        F.flce_forward(x, W, b, y, workspace=fws, out=(loss, lse), gemm_form=form, kept=kept,
-                       bwd_vocab_block=1024, **opts)
+        F.flce_forward(x, W, b, y, workspace=fws, out=(loss, lse), gemm_form=form,
+                       bwd_vocab_block=1024, **state, **opts)
         F.flce_backward(dloss, lse, x, W, b, y, workspace=bws, out=(dx, dW, db),
-                        gemm_form=form, kept=kept, bwd_vocab_block=1024, **opts)
+                        gemm_form=form, bwd_vocab_block=1024, **state, **opts)
 
     def snapshot():
         torch.cuda.synchronize(dev)

@@ -25,19 +25,23 @@ def _sim_allreduce(tensors):
     return run
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("mode", ["recompute", "kept"])
 @pytest.mark.parametrize("form", ["default", "single", "wide"])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
-def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, monkeypatch):
+def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, dtype, monkeypatch):
     # The shard calls take no gemm_form of their own: the environment override
     # selects the kernel form for every call of the test (shard offsets in the
     # wide and single-CTA kernels as well as the default pairs).
     if form != "default":
         monkeypatch.setenv("FLCE_GEMM_FORM", form)
+    # fp16: as in fp16 training, a loss scale keeps the fp16 dx above fp16's
+    # subnormals.
     wl = I.Workload("vp", N=300, H=264, V=3001, seed=41, b_std=0.3, ignore_frac=0.1,
                     label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.8,
                     reduction=reduction,
-                    dloss="normal_per_token" if reduction == "none" else "normal_scalar")
+                    dloss="normal_per_token" if reduction == "none" else "normal_scalar",
+                    dtype=dtype, dloss_scale=1024.0 if dtype == "fp16" else 1.0)
     inp = I.make_inputs(wl)
     prob = DeviceProblem(inp)
     opts = opts_of(wl)
@@ -70,7 +74,7 @@ def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, monkeypatch
              for (a, n), k in zip(shards, kept)]
     dx32 = [p[0] for p in parts]
     _sim_allreduce(dx32)("sum")
-    dx = VP.cast16(dx32[0])
+    dx = VP.cast16(dx32[0], prob.x.dtype)
     dW = torch.cat([p[1] for p in parts])
     db = torch.cat([p[2] for p in parts])
     torch.cuda.synchronize()
