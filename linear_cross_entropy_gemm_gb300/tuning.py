@@ -128,6 +128,21 @@ def _event_timer(fn: Callable[[], None], reps: int, warmup: int) -> float:
     return statistics.median(times)
 
 
+def _interleaved(cands: Dict, timer: Callable[[Callable[[], None], int, int], float], reps: int,
+                 warmup: int) -> Dict:
+    """Median time per candidate, measured round-robin: every candidate is
+    warmed up, then each repetition times every candidate once, so a drift of
+    the GPU's clock (at the power cap it moves with temperature and the power
+    history) falls on all candidates alike instead of on whichever ran last."""
+    for fn in cands.values():
+        timer(fn, 1, warmup)
+    times = {k: [] for k in cands}
+    for _ in range(reps):
+        for k, fn in cands.items():
+            times[k].append(timer(fn, 1, 0))
+    return {k: statistics.median(v) for k, v in times.items()}
+
+
 def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: torch.Tensor, *,
              dloss: Optional[torch.Tensor] = None, ignore_index: int = -100,
              label_smoothing: float = 0.0, lse_square_scale: float = 0.0,
@@ -138,8 +153,8 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
              use_cache: bool = True, mode: str = "recompute",
              timer: Callable[[Callable[[], None], int, int], float] = _event_timer) -> TuneResult:
     """Time flce_forward per GEMM form and the backward per (form, BVc) on
-    these tensors and return the fastest configuration (cached per
-    ``problem_key``). mode "recompute" times flce_backward alone; mode "kept"
+    these tensors, candidates interleaved round-robin (``_interleaved``), and
+    return the fastest configuration (cached per ``problem_key``). mode "recompute" times flce_backward alone; mode "kept"
     times, per (form, BVc), the kept-block forward + backward pair (the kept
     block is BVc wide, so the pair is what the block choice changes), and
     backward_ms then holds those pair times. Allocates one set of outputs and
@@ -181,11 +196,10 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
     dW = torch.empty(V, H, dtype=dW_dtype, device=dev)
     db = torch.empty(V, dtype=db_dtype, device=dev) if b is not None else None
 
-    forward_ms = {}
-    for form in forms:
-        forward_ms[form] = timer(
-            lambda form=form: flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse),
-                                           gemm_form=form, **opts), reps, warmup)
+    forward_ms = _interleaved(
+        {form: (lambda form=form: flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse),
+                                               gemm_form=form, **opts)) for form in forms},
+        timer, reps, warmup)
     flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse), **opts)
     def kept_pair(form, bv):
         flce_forward(x, W, b, y, workspace=ws_f, out=(loss, lse), gemm_form=form, kept=kept_buf,
@@ -194,7 +208,7 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
                       bwd_vocab_block=bv, workspace=ws_b, out=(dx, dW, db), gemm_form=form,
                       kept=kept_buf, **opts)
 
-    backward_ms = {}
+    cands = {}
     for form in forms:
         for bv in blocks:
             if kept:
@@ -204,7 +218,8 @@ def autotune(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: tor
                     dloss, lse, x, W, b, y, dW_dtype=dW_dtype, db_dtype=db_dtype,
                     bwd_vocab_block=bv, workspace=ws_b, out=(dx, dW, db),
                     gemm_form=form, **opts)
-            backward_ms[(form, int(bv))] = timer(fn, reps, warmup)
+            cands[(form, int(bv))] = fn
+    backward_ms = _interleaved(cands, timer, reps, warmup)
     result = TuneResult(config=select(forward_ms, backward_ms), forward_ms=forward_ms,
                         backward_ms=backward_ms, key=key)
     if use_cache:

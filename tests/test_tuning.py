@@ -127,3 +127,19 @@ def test_full_size_samples_cover_the_default_seams(name):
     cols_s = I.sample_indices(wl.seed + 1, wl.V, 256, must_include=sorted(cols))
     assert len(rows_s) == 256 and len(cols_s) == 256
     assert rows <= set(rows_s.tolist()) and cols <= set(cols_s.tolist())
+
+
+def test_interleaved_timing_round_robins_the_candidates():
+    # Every candidate is warmed up once, then timed once per repetition in a
+    # fixed rotation; the result is each candidate's median.
+    calls = []
+
+    def timer(fn, reps, warmup):
+        calls.append((fn(), reps, warmup))
+        return {"a": [5.0, 1.0, 3.0], "b": [2.0, 2.0, 9.0]}[calls[-1][0]][
+            sum(1 for c in calls[:-1] if c[0] == calls[-1][0] and c[1:] == (1, 0))]
+
+    res = tuning._interleaved({"a": lambda: "a", "b": lambda: "b"}, timer, reps=3, warmup=2)
+    assert [c for c in calls[:2]] == [("a", 1, 2), ("b", 1, 2)]
+    assert [c[0] for c in calls[2:]] == ["a", "b", "a", "b", "a", "b"]
+    assert res == {"a": 3.0, "b": 2.0}
