@@ -7,7 +7,7 @@ V=128256, bf16, mean reduction, no bias, dloss = 1. Prints ONE JSON line
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload tiny|medium|llama3_head|large_logit|vocab256k]
-                  [--mode kept|recompute|stored]
+                  [--mode kept|recompute|stored|budget]
 
 * value: tokens/s over all ranks, inputs resident in HBM, device time per
   step from CUDA events on the launching stream; L2 flushed (256 MiB write)
@@ -16,8 +16,12 @@ V=128256, bf16, mean reduction, no bias, dloss = 1. Prints ONE JSON line
   autograd module's): the forward keeps the first backward vocabulary
   block's probabilities in the buffer the backward stages dL in, and the
   backward recomputes the other blocks. "recompute": every block recomputed.
-  "stored": every logit's probability kept (2 N V bytes more memory). The
-  two other modes are timed the same way and reported in "modes".
+  "stored": every logit's probability kept (2 N V bytes more memory).
+  "budget": the kept block as wide as the method's memory budget allows
+  (flce_keep_vocab_within: kept-mode memory within the recompute mode's
+  plus an fp32 [V, H] dW accumulator, which this library never allocates).
+  The other modes are timed the same way and reported in "modes" ("budget"
+  only where its kept block is neither one block nor the whole vocabulary).
 * e2e: the same metric through the C ABI with the step's inputs (x, y,
   dloss) copied from pinned host memory and the loss read back every step;
   the next step's copy runs on a side stream during the current step. The
@@ -79,7 +83,7 @@ METRIC = "FLCE fwd+bwd ms, tokens/s, TFLOP/s (% bf16 TC peak) @ 8192×4096×1282
 HEADLINE = "llama3_head"
 PAGES_MS = 19.897  # Liger-Kernel commit 95b01e9, B200, Llama-3 head shape (context)
 L2_FLUSH_BYTES = 256 << 20
-MODES = ("kept", "recompute", "stored")
+MODES = ("kept", "recompute", "stored", "budget")
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, averaged over a
 # step's launches of each kernel, from one ncu capture of the Llama-3 head
 # step in the kept-block mode (1-pass metrics, default GEMM forms and block,
@@ -312,6 +316,20 @@ class Problem:
         self.tdt = tdt
         self.bufs = None
 
+    def keep_vocab(self, mode):
+        """keep_vocab of a mode: the budget width for "budget", else 0."""
+        if mode != "budget":
+            return 0
+        wl = self.wl
+        return self.F.flce_keep_vocab_within(wl.N, wl.H, wl.V, has_bias=wl.has_bias,
+                                             bwd_vocab_block=self.bkw.get("bwd_vocab_block", 0))
+
+    def kept_cols(self, mode, bv):
+        """Vocabulary columns whose logits the backward does not recompute."""
+        V = self.wl.V
+        return {"recompute": 0, "kept": min(bv, V), "stored": V,
+                "budget": min(self.keep_vocab("budget"), V)}[mode]
+
     def allocate(self, mode):
         torch, F, wl = self.torch, self.F, self.wl
         N, H, V, dev = wl.N, wl.H, wl.V, self.dev
@@ -330,21 +348,24 @@ class Problem:
             return self.bufs
         bvb = self.bkw.get("bwd_vocab_block", 0)
         fp16 = self.tdt == torch.float16
-        b = {"mode": mode}
+        kv = self.keep_vocab(mode)
+        b = {"mode": mode, "keep_vocab": kv}
         b["fws"] = torch.empty(F.flce_workspace_size(N, H, V, "forward", **self.opts),
                                dtype=torch.uint8, device=dev)
-        kind = {"kept": "backward_keep", "stored": "backward_store"}.get(mode, "backward")
+        kind = {"kept": "backward_keep", "budget": "backward_keep",
+                "stored": "backward_store"}.get(mode, "backward")
         b["bws"] = torch.empty(F.flce_workspace_size(N, H, V, kind, bwd_vocab_block=bvb,
-                                                     has_bias=wl.has_bias, **self.opts),
+                                                     has_bias=wl.has_bias, keep_vocab=kv,
+                                                     **self.opts),
                                dtype=torch.uint8, device=dev)
         b["state"] = None
         if mode == "stored":
             b["state"] = torch.empty(F.flce_saved_size(N, H, V, input_fp16=fp16, **self.opts),
                                      dtype=torch.uint8, device=dev)
-        elif mode == "kept":
+        elif mode in ("kept", "budget"):
             b["state"] = torch.empty(F.flce_kept_size(N, H, V, input_fp16=fp16,
-                                                      bwd_vocab_block=bvb), dtype=torch.uint8,
-                                     device=dev)
+                                                      bwd_vocab_block=bvb, keep_vocab=kv),
+                                     dtype=torch.uint8, device=dev)
         b["loss"] = torch.empty(N if wl.reduction == "none" else 1, dtype=torch.float32, device=dev)
         b["lse"] = torch.empty(N, dtype=torch.float32, device=dev)
         b["dx"] = torch.empty(N, H, dtype=self.tdt, device=dev)
@@ -383,6 +404,8 @@ class Problem:
             return
         st = {} if b["state"] is None else {("saved" if b["mode"] == "stored" else "kept"):
                                             b["state"]}
+        if b["mode"] == "budget":
+            st["keep_vocab"] = b["keep_vocab"]
         F.flce_forward(xb, self.W, self.b, yb, workspace=b["fws"], out=(b["loss"], b["lse"]),
                        trace=ftr, bwd_vocab_block=self.bkw.get("bwd_vocab_block", 0),
                        **st, **self.opts, **self.fkw)
@@ -438,12 +461,12 @@ def end_to_end(torch, stream, prob, steps, barrier):
     return e0.elapsed_time(e1) / steps, h2d_bytes, host_loss.numel() * 4
 
 
-def kernel_flops(name, wl, bv, mode):
-    """Algorithmic flops per step of each GEMM kernel in a backward mode."""
+def kernel_flops(name, wl, kept_cols):
+    """Algorithmic flops per step of each GEMM kernel when the backward
+    recomputes all but `kept_cols` vocabulary columns."""
     N, H, V = wl.N, wl.H, wl.V
-    kept_cols = min(bv, V) if mode == "kept" else 0
     f = {"fwd_lse": 2.0 * N * H * V, "bwd_dw": 2.0 * N * H * V, "bwd_dx": 2.0 * N * H * V}
-    if mode != "stored":
+    if kept_cols < V:
         f["bwd_dlogits"] = 2.0 * N * H * (V - kept_cols)
     return f.get(name)
 
@@ -499,7 +522,7 @@ def run_ours(args):
     shard = None
     if vocab_split:
         from linear_cross_entropy_gemm_gb300 import vocab_parallel as VP
-        if args.autotune or V < 256 * ws or args.mode == "stored":
+        if args.autotune or V < 256 * ws or args.mode in ("stored", "budget"):
             raise SystemExit("--parallel vocab: kept or recompute mode, no autotuning, and "
                              "V >= 256 per rank")
         args.only_mode = True
@@ -523,7 +546,11 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    modes = [args.mode] + ([] if args.only_mode else [m for m in MODES if m != args.mode])
+    bv_default = bvb or tuning.library_default_block(N, V)
+    distinct = {"budget": prob.kept_cols("budget", bv_default)
+                not in (min(bv_default, V), V)}
+    modes = [args.mode] + ([] if args.only_mode else
+                           [m for m in MODES if m != args.mode and distinct.get(m, True)])
     results = {}
     for mode in modes:
         # Memory: everything allocated above the live inputs across one step.
@@ -564,7 +591,8 @@ def run_ours(args):
                 "share": sum(v) / sum(totals.values())} for k, v in sorted(per_kernel.items())}
     dom = max(totals, key=totals.get) if totals else None
     dom_ms = totals[dom] / steps_ if totals else None
-    dom_flops = kernel_flops(dom, wl, bv_used, args.mode) if totals else None
+    kept_cols = prob.kept_cols(args.mode, bv_used) if shard is None else None
+    dom_flops = kernel_flops(dom, wl, kept_cols) if totals else None
     v_local = V if shard is None else shard[1] - shard[0]
     if vocab_split:
         # The shard calls are not traced per kernel: the roofline is the whole
@@ -608,7 +636,7 @@ def run_ours(args):
         kept_cols = min(tuning.library_default_block(N, v_local) if not bvb else bvb, v_local)
         executed = 8.0 * N * H * v_local - (2.0 * N * H * kept_cols if args.mode == "kept" else 0)
     else:
-        executed = sum(kernel_flops(k, wl, bv_used, args.mode) or 0.0 for k in totals)
+        executed = sum(kernel_flops(k, wl, kept_cols) or 0.0 for k in totals)
     tflops = flops_8 / (ms * 1e-3) / 1e12
     # Replicas: every rank runs the whole workload. Vocabulary split: the
     # ranks run one workload together.
@@ -619,6 +647,7 @@ def run_ours(args):
         if m == args.mode:
             continue
         other[m] = {"ms_per_step": r["ms"], "value": ws * N / (r["ms"] * 1e-3),
+                    "keep_vocab": prob.keep_vocab(m) or None,
                     "unit": "tokens/s", "tflops_8nhv_equivalent": flops_8 / (r["ms"] * 1e-3) / 1e12,
                     "memory": r["mem"], "loss": r["loss"],
                     "kernels": {k: {"launches_per_step": len(v) // steps_,
@@ -628,10 +657,12 @@ def run_ours(args):
         # The library's scratch bound: one [N, BVc] 16-bit block (dL staging,
         # or the kept probabilities) and the kept block's per-32-column maxima,
         # the fp32 dx accumulator, the db column partials (with a bias), the
-        # forward's per-tile partials and the per-token coefficients.
+        # forward's per-tile partials and the per-token coefficients; in the
+        # budget mode plus the fp32 [V, H] allowance its kept block may use.
         "scratch_bound_mib": (N * bv_used * 2 + N * (bv_used // 32) * 4 + N * H * 4
                               + (4 * -(-N // 128) * bv_used * 4 if wl.has_bias else 0)
-                              + N * -(-V // 256) * 12 + N * 32) / 2**20 + 1,
+                              + N * -(-V // 256) * 12 + N * 32
+                              + (V * H * 4 if args.mode == "budget" else 0)) / 2**20 + 1,
         # The method's memory budget, one [N, BV] block set plus an fp32
         # [V, H] dW accumulator, with BV the backward vocabulary block.
         "method_budget_mib": (N * bv_used * 2 + V * H * 4) / 2**20,
@@ -645,6 +676,7 @@ def run_ours(args):
         "dtype": wl.dtype, "data": "synthetic",
         "config": config_of(wl, ws, vocab_split),
         "impl_config": {"mode": args.mode, "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
+                        "keep_vocab": (prob.keep_vocab(args.mode) if shard is None else 0) or None,
                         "gemm_form": forms_used,
                         **({"vocab_shard": list(shard)} if vocab_split else {})},
         "loss": head["loss"],

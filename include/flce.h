@@ -105,6 +105,10 @@ typedef struct {
   int32_t input_fp16;       /* 0: x, W, b are bf16; 1: they are fp16 (dx, and dW / db when
                                not fp32, are then fp16 too) */
   int32_t gemm_form;        /* flce_gemm_form_t; 0 = library default */
+  int64_t keep_vocab;       /* kept-block calls only: width of the kept block, the
+                               vocabulary columns [0, keep_vocab) whose probabilities
+                               the forward keeps (a multiple of 256; 0 = BVc; values
+                               below BVc keep BVc, values >= V the whole vocabulary) */
 } flce_params_t;
 
 /* Kernel kinds reported by the traced entry points. */
@@ -197,22 +201,43 @@ flce_status_t flce_backward_traced(const flce_params_t* p, const float* dloss, c
  * caller's `kept` buffer (flce_kept_size(p) bytes, 16-byte aligned), the
  * probabilities of the first backward vocabulary block [0, BVc), where BVc is
  * the block flce_backward would use for p (bwd_vocab_block, or the library
- * default): each 32-column chunk's q = exp(z - m_c) as fp16 in an [N, BVc]
- * array, m_c being the running maximum of the row's logits up to that chunk,
- * plus the m_c (fp32). These are exponentials the forward's online softmax
- * computes anyway. flce_backward_keep turns that block into its dlogits in
- * place (an HBM pass instead of 2 N H BVc flops of recompute) and then uses
- * the same buffer as the dL staging block of the blocks it recomputes, so
- * its workspace (flce_workspace_size(p, 2)) holds no dL block: the kept
- * buffer plus that workspace take the same memory as flce_backward's
- * workspace. At the Llama-3 head shape (V = 128256, BVc = 65536) this skips
- * half of the recompute, an eighth of the step's flops.
- * Both calls take the same p (the kept layout depends on N, V and BVc); the
- * backward consumes the kept state (it holds dL afterwards), and the buffer
- * must be left untouched between the two calls. The vocabulary-shard calls
- * have kept-block forms too (below). trace may be NULL.
+ * default; p->keep_vocab widens the kept block, below): each 32-column
+ * chunk's q = exp(z - m_c) as fp16 in an [N, BVc] array, m_c being the
+ * running maximum of the row's logits up to that chunk, plus the m_c (fp32).
+ * These are exponentials the forward's online softmax computes anyway.
+ * flce_backward_keep turns that block into its dlogits in place (an HBM pass
+ * instead of 2 N H BVc flops of recompute) and then uses the same buffer as
+ * the dL staging block of the blocks it recomputes, so its workspace
+ * (flce_workspace_size(p, 2)) holds no dL block: the kept buffer plus that
+ * workspace take the same memory as flce_backward's workspace, plus the
+ * chunk maxima. At the Llama-3 head shape (V = 128256, BVc = 65536) this
+ * skips half of the recompute, an eighth of the step's flops.
+ * Both calls take the same p (the kept layout depends on N, V, BVc and
+ * keep_vocab); the backward consumes the kept state (it holds dL
+ * afterwards), and the buffer must be left untouched between the two calls.
+ * The vocabulary-shard calls have kept-block forms too (below). trace may be
+ * NULL.
  */
 size_t flce_kept_size(const flce_params_t* p);
+
+/* A wider kept block (p->keep_vocab > BVc) trades memory for recompute: the
+ * forward keeps the probabilities of [0, K) (K = keep_vocab, capped at the
+ * vocabulary), the backward converts that block in place and then recomputes
+ * the rest, [K, V), in blocks of BVc staged at the start of the kept buffer.
+ * K = V is the stored mode below. flce_kept_size and
+ * flce_workspace_size(p, 2) follow keep_vocab.
+ *
+ * flce_keep_vocab_within returns the widest keep_vocab whose kept-mode
+ * memory, flce_kept_size + flce_workspace_size(., 2), stays within
+ * flce_workspace_size(p, 1) + extra_bytes (the recompute backward's
+ * workspace plus extra_bytes). The widths tried are the whole vocabulary,
+ * then V - k BVc rounded up to 256 for k = 1, 2, ... (so the recomputed part
+ * is k blocks of BVc at most), down to BVc, which is returned when nothing
+ * wider fits (one block takes N BVc / 8 bytes of chunk maxima more than the
+ * recompute mode). extra_bytes = 4 V H is the fp32 [V, H] dW accumulator
+ * that the method's memory budget allows for and this library never
+ * allocates. Host only; returns 0 for invalid parameters or N == 0. */
+int64_t flce_keep_vocab_within(const flce_params_t* p, size_t extra_bytes);
 flce_status_t flce_forward_keep(const flce_params_t* p, const void* x, const void* W,
                                 const void* b, const int64_t* y, float* loss, float* lse,
                                 void* kept, size_t kept_bytes, void* workspace,
@@ -227,7 +252,8 @@ flce_status_t flce_backward_keep(const flce_params_t* p, const float* dloss, con
 /*
  * Stored-probability mode: no logits recompute in the backward pass. This is
  * the kept-block mode with one block spanning the whole vocabulary
- * (p->bwd_vocab_block is ignored): flce_forward_store keeps every logit's
+ * (p->bwd_vocab_block and p->keep_vocab are ignored): flce_forward_store
+ * keeps every logit's
  * probability, ~2 N V bytes in `saved` (flce_saved_size(p) bytes, 16-byte
  * aligned), and flce_backward_store converts it to dlogits in place and runs
  * one dW and one dx GEMM over the whole vocabulary, saving 2 N H V flops (a

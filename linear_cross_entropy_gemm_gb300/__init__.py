@@ -27,7 +27,7 @@ __all__ = [
     "flce_forward", "flce_backward", "flce_workspace_size", "flce_read_device_error",
     "FusedLinearCrossEntropyFunction", "FusedLinearCrossEntropyLoss",
     "fused_linear_cross_entropy", "FlceError", "params", "KernelTrace", "flce_saved_size",
-    "GEMM_FORMS", "resolved_gemm_form", "flce_kept_size",
+    "GEMM_FORMS", "resolved_gemm_form", "flce_kept_size", "flce_keep_vocab_within",
 ]
 
 _err_words = {}
@@ -131,11 +131,27 @@ def flce_saved_size(N, H, V, **opts) -> int:
 
 def flce_kept_size(N, H, V, **opts) -> int:
     """Bytes of the state flce_forward(..., kept=) leaves for the backward: the
-    first backward vocabulary block's fp16 probabilities [N, BVc] and the
-    running maxima of its 32-column chunks. It doubles as the backward's dL
-    staging block, so a kept-block forward + backward takes no more memory
-    than the plain pair."""
+    kept block's fp16 probabilities [N, K] (K = ``keep_vocab``, by default one
+    backward vocabulary block BVc) and the running maxima of its 32-column
+    chunks. It doubles as the backward's dL staging block, so with one block a
+    kept-block forward + backward takes the memory of the plain pair plus the
+    chunk maxima."""
     return int(_lib.load().flce_kept_size(params(N, H, V, **opts)))
+
+
+def flce_keep_vocab_within(N, H, V, extra_bytes: Optional[int] = None, **opts) -> int:
+    """The widest kept block (``keep_vocab``) whose kept-mode memory (kept
+    state + backward workspace) is at most the recompute backward's workspace
+    plus ``extra_bytes``; at least one backward block. The default extra is
+    4 V H bytes: the fp32 [V, H] dW accumulator that the method's memory budget
+    allows for and this library never allocates."""
+    extra = 4 * int(V) * int(H) if extra_bytes is None else int(extra_bytes)
+    if extra < 0:
+        raise ValueError("flce: extra_bytes must be >= 0")
+    k = int(_lib.load().flce_keep_vocab_within(params(N, H, V, **opts), extra))
+    if k <= 0:
+        raise ValueError("flce: invalid parameters")
+    return k
 
 
 def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y: torch.Tensor, *,
@@ -146,7 +162,8 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
                  stream=None, trace: Optional[KernelTrace] = None,
                  saved: Optional[torch.Tensor] = None,
                  gemm_form="default", kept: Optional[torch.Tensor] = None,
-                 bwd_vocab_block: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+                 bwd_vocab_block: int = 0, keep_vocab: int = 0
+                 ) -> Tuple[torch.Tensor, torch.Tensor]:
     """Loss and per-token lse. loss is a 0-dim fp32 tensor (sum/mean) or [N]
     fp32 (none); lse is [N] fp32. Runs on the current stream, no sync.
     With ``saved`` (a uint8 CUDA tensor of flce_saved_size bytes) the forward
@@ -157,9 +174,11 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
     flce_workspace_size(..., "forward") bytes; when it is not given, or is
     smaller, a new one is allocated for the call.
     With ``kept`` (a uint8 CUDA tensor of flce_kept_size bytes; give the
-    backward's ``bwd_vocab_block`` here too) the forward also leaves the first
-    backward vocabulary block's probabilities for flce_backward(..., kept=),
-    which then skips that block's recompute."""
+    backward's ``bwd_vocab_block`` and ``keep_vocab`` here too) the forward
+    also leaves the kept block's probabilities for flce_backward(..., kept=),
+    which then skips that block's recompute. The kept block is the vocabulary
+    columns [0, keep_vocab) (a multiple of 256; 0 = one backward block; see
+    flce_keep_vocab_within)."""
     _check_inputs(x, W, b, y)
     lib = _lib.load()
     N, H = x.shape
@@ -170,7 +189,7 @@ def flce_forward(x: torch.Tensor, W: torch.Tensor, b: Optional[torch.Tensor], y:
                lse_square_scale=lse_square_scale, logit_scale=logit_scale,
                reduction=reduction, has_bias=b is not None,
                input_fp16=x.dtype == torch.float16, gemm_form=gemm_form,
-               bwd_vocab_block=bwd_vocab_block)
+               bwd_vocab_block=bwd_vocab_block, keep_vocab=keep_vocab)
     dev = x.device
     if out is not None:
         loss, lse = out
@@ -204,14 +223,14 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                   bwd_vocab_block: int = 0, workspace: Optional[torch.Tensor] = None,
                   out: Optional[Tuple] = None, stream=None, trace: Optional[KernelTrace] = None,
                   saved: Optional[torch.Tensor] = None, gemm_form="default",
-                  kept: Optional[torch.Tensor] = None):
+                  kept: Optional[torch.Tensor] = None, keep_vocab: int = 0):
     """dx [N, H] bf16, dW [V, H] (dW_dtype fp32 or bf16), db [V] or None.
     With ``saved`` (filled by flce_forward(..., saved=)) the logits are not
     recomputed: dlogits come from the stored tile probabilities. With
-    ``kept`` (filled by flce_forward(..., kept=) with the same options and
-    ``bwd_vocab_block``) the first vocabulary block's dlogits come from the
-    kept probabilities and the buffer stages every block's dL; the call
-    consumes it.
+    ``kept`` (filled by flce_forward(..., kept=) with the same options,
+    ``bwd_vocab_block`` and ``keep_vocab``) the kept block's dlogits come
+    from the kept probabilities and the buffer stages every block's dL; the
+    call consumes it.
     ``bwd_vocab_block`` (0 = library default) and ``gemm_form`` select the
     vocabulary block and GEMM form; see ``tuning.autotune``. ``workspace``: as
     in flce_forward, with flce_workspace_size(..., "backward") bytes."""
@@ -234,7 +253,7 @@ def flce_backward(dloss: torch.Tensor, lse: torch.Tensor, x: torch.Tensor, W: to
                reduction=reduction, has_bias=b is not None,
                dW_fp32=dW_dtype == torch.float32, db_fp32=db_dtype == torch.float32,
                bwd_vocab_block=bwd_vocab_block, input_fp16=x.dtype == torch.float16,
-               gemm_form=gemm_form)
+               gemm_form=gemm_form, keep_vocab=keep_vocab)
     if out is not None:
         dx, dW, db = out
     else:
@@ -286,34 +305,54 @@ def flce_read_device_error(device=None, stream=None) -> int:
     return int(h.value)
 
 
+def _keep_width(keep_vocab, N, H, V, bias, x, bwd_vocab_block) -> int:
+    """keep_vocab as the library takes it: 0 (one backward block), a column
+    count rounded up to a multiple of 256, or "budget"
+    (flce_keep_vocab_within with the method's fp32 dW accumulator allowance)."""
+    if keep_vocab == "budget":
+        return flce_keep_vocab_within(N, H, V, has_bias=bias is not None,
+                                      input_fp16=x.dtype == torch.float16,
+                                      bwd_vocab_block=bwd_vocab_block)
+    if isinstance(keep_vocab, str) or int(keep_vocab) < 0:
+        raise ValueError(f"keep_vocab: 0, a column count or 'budget', got {keep_vocab!r}")
+    return (int(keep_vocab) + 255) // 256 * 256
+
+
 class FusedLinearCrossEntropyFunction(torch.autograd.Function):
     """Autograd wrapper. By default the forward keeps lse and the first
     backward vocabulary block's probabilities (the buffer the backward stages
-    dL in, so no extra memory) and the backward recomputes the other blocks'
-    logits; keep_block=False recomputes every block; recompute=False keeps
-    every logit's probability (~2 N V bytes) and recomputes none."""
+    dL in, so no extra memory but the chunk maxima) and the backward
+    recomputes the other blocks' logits; keep_vocab widens the kept block
+    (a column count, or "budget": the widest within the method's memory
+    budget, see flce_keep_vocab_within); keep_block=False recomputes every
+    block; recompute=False keeps every logit's probability (~2 N V bytes) and
+    recomputes none."""
 
     @staticmethod
     def forward(ctx, x, target, weight, bias=None, ignore_index=-100, label_smoothing=0.0,
                 lse_square_scale=0.0, logit_scale=1.0, reduction="mean", recompute=True,
-                config=None, keep_block=True):
+                config=None, keep_block=True, keep_vocab=0):
         saved = kept = None
         N, H, V = x.shape[0], x.shape[1], weight.shape[0]
         bwd_kw = {} if config is None else config.backward_kwargs()
+        bvb = bwd_kw.get("bwd_vocab_block", 0)
+        kv = 0
         if not recompute:
             n = flce_saved_size(N, H, V, label_smoothing=label_smoothing,
                                 input_fp16=x.dtype == torch.float16)
             saved = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
         elif keep_block and N > 0:
+            kv = _keep_width(keep_vocab, N, H, V, bias, x, bvb)
             n = flce_kept_size(N, H, V, input_fp16=x.dtype == torch.float16,
-                               bwd_vocab_block=bwd_kw.get("bwd_vocab_block", 0))
+                               bwd_vocab_block=bvb, keep_vocab=kv)
             kept = torch.empty(max(n, 1), dtype=torch.uint8, device=x.device)
         ctx.config = config
+        ctx.keep_vocab = kv
         loss, lse = flce_forward(x, weight, bias, target, ignore_index=ignore_index,
                                  label_smoothing=label_smoothing,
                                  lse_square_scale=lse_square_scale, logit_scale=logit_scale,
                                  reduction=reduction, saved=saved, kept=kept,
-                                 bwd_vocab_block=bwd_kw.get("bwd_vocab_block", 0),
+                                 bwd_vocab_block=bvb, keep_vocab=kv,
                                  **({} if config is None else config.forward_kwargs()))
         ctx.saved_state = saved
         ctx.kept_state = kept
@@ -328,22 +367,25 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
         x, target, weight, bias, lse = ctx.saved_tensors
         dx, dW, db = flce_backward(dloss.float().contiguous(), lse, x, weight, bias, target,
                                    dW_dtype=torch.float32, db_dtype=torch.float32,
-                                   saved=ctx.saved_state, kept=ctx.kept_state, **ctx.opts,
+                                   saved=ctx.saved_state, kept=ctx.kept_state,
+                                   keep_vocab=ctx.keep_vocab, **ctx.opts,
                                    **({} if ctx.config is None else ctx.config.backward_kwargs()))
         ctx.saved_state = ctx.kept_state = None
         dW = dW.to(weight.dtype)
         db = None if db is None else db.to(bias.dtype)
-        return dx, None, dW, db, None, None, None, None, None, None, None, None
+        return dx, None, dW, db, None, None, None, None, None, None, None, None, None
 
 
 def fused_linear_cross_entropy(x, target, weight, bias=None, ignore_index=-100,
                                label_smoothing=0.0, lse_square_scale=0.0, logit_scale=1.0,
                                reduction="mean", recompute=True, config=None,
-                               keep_block=True):
+                               keep_block=True, keep_vocab=0):
     """Functional form; x [N, H] bf16, target [N] int64, weight [V, H] bf16.
     By default the forward keeps the first backward vocabulary block's
     probabilities in the buffer the backward stages dL in (no extra memory),
     so the backward recomputes the logits of the other blocks only;
+    keep_vocab widens the kept block: a column count, or "budget" for the
+    widest within the method's memory budget (flce_keep_vocab_within).
     keep_block=False recomputes all. recompute=False keeps fp16 tile
     probabilities of every logit (~2 N V bytes) so the backward skips the
     logits GEMM. ``config``: a ``tuning.FlceConfig`` (GEMM forms, backward
@@ -351,7 +393,7 @@ def fused_linear_cross_entropy(x, target, weight, bias=None, ignore_index=-100,
     return FusedLinearCrossEntropyFunction.apply(x, target, weight, bias, ignore_index,
                                                  label_smoothing, lse_square_scale,
                                                  logit_scale, reduction, recompute, config,
-                                                 keep_block)
+                                                 keep_block, keep_vocab)
 
 
 class FusedLinearCrossEntropyLoss(torch.nn.Module):
@@ -359,7 +401,7 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
 
     def __init__(self, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
                  logit_scale=1.0, reduction="mean", recompute=True, autotune=False,
-                 keep_block=True):
+                 keep_block=True, keep_vocab=0):
         """autotune=True: the first call for each (shape, dtype, options) key
         times the GEMM forms and backward vocabulary blocks on the caller's
         tensors (tuning.autotune) and later calls reuse the fastest."""
@@ -374,6 +416,7 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         self.recompute = recompute
         self.autotune = autotune
         self.keep_block = keep_block
+        self.keep_vocab = keep_vocab
 
     def forward(self, x, target, weight, bias=None):
         x2 = x.reshape(-1, x.shape[-1]).contiguous()
@@ -390,4 +433,4 @@ class FusedLinearCrossEntropyLoss(torch.nn.Module):
         return fused_linear_cross_entropy(
             x2, y2, weight, bias, self.ignore_index, self.label_smoothing,
             self.lse_square_scale, self.logit_scale, self.reduction, self.recompute, config,
-            self.keep_block)
+            self.keep_block, self.keep_vocab)

@@ -43,6 +43,7 @@ class FlceParams(ctypes.Structure):
         ("vocab_total", ctypes.c_int64),
         ("input_fp16", ctypes.c_int32),
         ("gemm_form", ctypes.c_int32),
+        ("keep_vocab", ctypes.c_int64),
     ]
 
 
@@ -104,6 +105,8 @@ def load() -> ctypes.CDLL:
     lib.flce_backward_store.restype = ctypes.c_int
     lib.flce_kept_size.argtypes = [P]
     lib.flce_kept_size.restype = sz
+    lib.flce_keep_vocab_within.argtypes = [P, sz]
+    lib.flce_keep_vocab_within.restype = ctypes.c_int64
     lib.flce_forward_keep.argtypes = lib.flce_forward_store.argtypes
     lib.flce_forward_keep.restype = ctypes.c_int
     lib.flce_backward_keep.argtypes = lib.flce_backward_store.argtypes
@@ -140,7 +143,7 @@ def load() -> ctypes.CDLL:
 def params(N, H, V, *, ignore_index=-100, label_smoothing=0.0, lse_square_scale=0.0,
            logit_scale=1.0, reduction="mean", has_bias=False, dW_fp32=True, db_fp32=True,
            bwd_vocab_block=0, vocab_start=0, vocab_total=0, input_fp16=False,
-           gemm_form="default") -> FlceParams:
+           gemm_form="default", keep_vocab=0) -> FlceParams:
     if reduction not in REDUCTION:
         raise ValueError(f"reduction must be one of {sorted(REDUCTION)}, got {reduction!r}")
     form = GEMM_FORMS.get(gemm_form, gemm_form) if isinstance(gemm_form, str) else int(gemm_form)
@@ -150,4 +153,4 @@ def params(N, H, V, *, ignore_index=-100, label_smoothing=0.0, lse_square_scale=
                       float(lse_square_scale), float(logit_scale), REDUCTION[reduction],
                       int(bool(has_bias)), int(bool(dW_fp32)), int(bool(db_fp32)),
                       int(bwd_vocab_block), int(vocab_start), int(vocab_total),
-                      int(bool(input_fp16)), form)
+                      int(bool(input_fp16)), form, int(keep_vocab))

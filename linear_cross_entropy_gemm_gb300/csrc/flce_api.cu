@@ -159,6 +159,7 @@ flce_status_t check_params(const flce_params_t* p) {
   if (!(p->lse_square_scale >= 0.f) || !(p->lse_square_scale < INFINITY)) return FLCE_ERR_INVALID_ARG;
   if (!(p->logit_scale > -INFINITY && p->logit_scale < INFINITY)) return FLCE_ERR_INVALID_ARG;
   if (p->bwd_vocab_block < 0 || p->bwd_vocab_block % 256 != 0) return FLCE_ERR_INVALID_ARG;
+  if (p->keep_vocab < 0 || p->keep_vocab % 256 != 0) return FLCE_ERR_INVALID_ARG;
   if (p->has_bias != 0 && p->has_bias != 1) return FLCE_ERR_INVALID_ARG;
   if (p->input_fp16 != 0 && p->input_fp16 != 1) return FLCE_ERR_INVALID_ARG;
   if (p->gemm_form < FLCE_GEMM_DEFAULT || p->gemm_form > FLCE_GEMM_WIDE_PAIR)
@@ -227,6 +228,31 @@ int64_t vocab_block(const flce_params_t* p) {
   return bv < vr ? bv : vr;
 }
 
+// Width of the kept block (the keep calls' first backward block): keep_vocab
+// columns, at least BVc (0 = BVc), at most the vocabulary rounded up to 256.
+int64_t kept_width(const flce_params_t* p) {
+  const int64_t bv = vocab_block(p);
+  const int64_t vr = (p->V + 255) / 256 * 256;
+  const int64_t k = p->keep_vocab > bv ? p->keep_vocab : bv;
+  return k < vr ? k : vr;
+}
+
+// Backward vocabulary blocks: [0, Vb0) is the kept block in the keep calls
+// (kept_width wide) and the first BVc block otherwise; the rest follow in
+// blocks of BVc, the last one ragged.
+struct Blocks {
+  int64_t first, bv;
+  int count;
+  Blocks(const flce_params_t* p, bool kept) : bv(vocab_block(p)) {
+    first = std::min<int64_t>(kept ? kept_width(p) : bv, p->V);
+    count = 1 + cdiv(p->V - first, bv);
+  }
+  int64_t start(int i) const { return i == 0 ? 0 : first + (i - 1) * bv; }
+  int64_t width(int i, int64_t V) const {
+    return i == 0 ? first : std::min<int64_t>(bv, V - start(i));
+  }
+};
+
 
 struct BwdWs {
   float4* coef;
@@ -237,24 +263,29 @@ struct BwdWs {
 };
 
 // kept: the backward of a kept-block forward stages dL in the kept buffer,
-// so its workspace holds no dL block.
+// so its workspace holds no dL block; its db column partials are as wide as
+// the kept block.
 size_t carve_bwd(const flce_params_t* p, void* base, BwdWs* w, bool kept = false) {
   const size_t N = static_cast<size_t>(p->N);
   const int64_t bv = vocab_block(p);
-  const int nblk = cdiv(p->V, bv);
+  const Blocks blocks(p, kept);
+  const int64_t db_cols = kept ? kept_width(p) : bv;
   Carver c(base, 0);
   w->coef = c.take<float4>(N);
   w->dl_scale = c.take<float>(2);
   w->dL = kept ? nullptr : c.take<uint16_t>(N * static_cast<size_t>(bv));
-  w->dx_acc = nblk > 1 ? c.take<float>(N * static_cast<size_t>(p->H)) : nullptr;
-  w->db_part = p->has_bias ? c.take<float>(static_cast<size_t>(cdiv(p->N, kBM)) * 4 * bv) : nullptr;
+  w->dx_acc = blocks.count > 1 ? c.take<float>(N * static_cast<size_t>(p->H)) : nullptr;
+  w->db_part = p->has_bias
+                   ? c.take<float>(static_cast<size_t>(cdiv(p->N, kBM)) * 4 * db_cols)
+                   : nullptr;
   return c.used() + kAlign;
 }
 
-// State kept between flce_forward_keep and flce_backward_keep: the first
-// backward vocabulary block's q [N, ld] (ld = BVc; the block's dL staging
-// buffer, converted in place) as fp16, then the running maxima of its
-// 32-column chunks [ceil(cols / 32), N] fp32.
+// State kept between flce_forward_keep and flce_backward_keep: the kept
+// block's q [N, ld] (ld = kept_width, cols = its columns inside the
+// vocabulary; converted in place into the block's dL, then the staging buffer
+// of the recomputed blocks) as fp16, then the running maxima of its 32-column
+// chunks [ceil(cols / 32), N] fp32.
 struct Kept {
   uint16_t* dq;
   float* kmax;
@@ -264,11 +295,11 @@ struct Kept {
 
 size_t carve_kept(const flce_params_t* p, void* base, Kept* k) {
   const size_t N = static_cast<size_t>(p->N);
-  const int64_t bv = vocab_block(p);
+  const int64_t kw = kept_width(p);
   Carver c(base, 0);
-  k->ld = bv;
-  k->cols = static_cast<int>(bv < p->V ? bv : p->V);
-  k->dq = c.take<uint16_t>(N * static_cast<size_t>(bv));
+  k->ld = kw;
+  k->cols = static_cast<int>(kw < p->V ? kw : p->V);
+  k->dq = c.take<uint16_t>(N * static_cast<size_t>(kw));
   k->kmax = c.take<float>(static_cast<size_t>(cdiv(k->cols, 32)) * N);
   return c.used() + kAlign;
 }
@@ -279,6 +310,7 @@ size_t carve_kept(const flce_params_t* p, void* base, Kept* k) {
 flce_params_t whole_vocab_block(const flce_params_t* p) {
   flce_params_t q = *p;
   q.bwd_vocab_block = (p->V + 255) / 256 * 256;
+  q.keep_vocab = 0;
   return q;
 }
 
@@ -436,6 +468,22 @@ size_t flce_kept_size(const flce_params_t* p) {
   if (check_params(p) != FLCE_OK || p->N == 0) return 0;
   Kept k{};
   return carve_kept(p, nullptr, &k);
+}
+
+int64_t flce_keep_vocab_within(const flce_params_t* p, size_t extra_bytes) {
+  if (check_params(p) != FLCE_OK || p->N == 0) return 0;
+  BwdWs w;
+  const size_t limit = carve_bwd(p, nullptr, &w, false) + extra_bytes;
+  const int64_t bv = vocab_block(p);
+  flce_params_t q = *p;
+  for (int64_t k = 0; p->V - k * bv > bv; ++k) {
+    q.keep_vocab = (p->V - k * bv + 255) / 256 * 256;
+    Kept kk{};
+    BwdWs wk;
+    if (carve_kept(&q, nullptr, &kk) + carve_bwd(&q, nullptr, &wk, true) <= limit)
+      return q.keep_vocab;
+  }
+  return bv;
 }
 
 flce_status_t flce_forward_keep(const flce_params_t* p, const void* x, const void* W,
@@ -656,12 +704,15 @@ static flce_status_t backward_impl(const char* name, const flce_params_t* p, con
   int sms = 0;
   if ((st = device_info(&sms)) != FLCE_OK) return st;
   carve_bwd(p, workspace, &w, kept != nullptr);
-  // The kept buffer is every block's dL staging buffer (same [N, BVc] layout).
+  // The kept buffer is every block's dL staging buffer: the kept block's own
+  // [N, ld] array, then [N, BVc] blocks at its start.
   if (kept) w.dL = kp.dq;
 
   const int N = static_cast<int>(p->N), H = static_cast<int>(p->H), V = static_cast<int>(p->V);
-  const int64_t bv = vocab_block(p);
-  const int nblk = cdiv(V, bv);
+  const Blocks blocks(p, kept != nullptr);
+  const int64_t bv = blocks.bv;
+  const int nblk = blocks.count;
+  const int ld_db = static_cast<int>(kept ? kp.ld : bv);
   int* derr = reinterpret_cast<int*>(dev_err);
   const GemmKind kind = gemm_kind(p);
   const bool pair = kind != kGemmSingle;
@@ -695,17 +746,19 @@ static flce_status_t backward_impl(const char* name, const flce_params_t* p, con
 
   for (int blk = 0; blk < nblk; ++blk) {
     NvtxRange nvtx_block("flce_backward_vocab_block");
-    const int v0 = static_cast<int>(blk * bv);
-    const int Vb = static_cast<int>(V - v0 < bv ? V - v0 : bv);
+    const int v0 = static_cast<int>(blocks.start(blk));
+    const int Vb = static_cast<int>(blocks.width(blk, V));
+    const bool from_kept = kept && blk == 0;
+    // Row pitch (elements) of this block's dL.
+    const int64_t ld = from_kept ? kp.ld : bv;
     CUtensorMap mdl_k, mdl_mn;
-    if (!encode_2d(&mdl_k, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, kBK, kBM, f16) ||
-        !encode_2d(&mdl_mn, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, 64, kBK, f16))
+    if (!encode_2d(&mdl_k, w.dL, Vb, N, static_cast<uint64_t>(ld) * 2, kBK, kBM, f16) ||
+        !encode_2d(&mdl_mn, w.dL, Vb, N, static_cast<uint64_t>(ld) * 2, 64, kBK, f16))
       return FLCE_ERR_CUDA;
 
     // Recompute the block's logits (or, for the kept block, read the kept
     // probabilities) and form dL (bf16) and db partials.
     int db_parts = 0;
-    const bool from_kept = kept && blk == 0;
     if (from_kept) {
       // In place: the kept q of block 0 becomes its dL.
       ConvertArgs ca;
@@ -719,11 +772,11 @@ static flce_status_t backward_impl(const char* name, const flce_params_t* p, con
       ca.v0 = 0;
       ca.Vb = Vb;
       ca.dL = w.dL;
-      ca.ld_dL = static_cast<int>(bv);
+      ca.ld_dL = static_cast<int>(ld);
       ca.fp16 = p->input_fp16;
       ca.dl_scale = w.dl_scale;
       ca.db_part = w.db_part;
-      ca.ld_db = static_cast<int>(bv);
+      ca.ld_db = ld_db;
       if (launch_convert(ca, s) != cudaSuccess || !tr.after(FLCE_KERNEL_BWD_CONVERT))
         return FLCE_ERR_CUDA;
       db_parts = convert_db_parts(N);
@@ -744,8 +797,8 @@ static flce_status_t backward_impl(const char* name, const flce_params_t* p, con
     da.v0 = v0;
     da.Vb = Vb;
     da.db_part = w.db_part;
-    da.ld_db = static_cast<int>(bv);
-    if (!encode_store_2d(&da.dl_map, w.dL, Vb, N, static_cast<uint64_t>(bv) * 2, false))
+    da.ld_db = ld_db;
+    if (!encode_store_2d(&da.dl_map, w.dL, Vb, N, static_cast<uint64_t>(ld) * 2, false))
       return FLCE_ERR_CUDA;
     if (!from_kept) {
       if (launch_dlogits(gemm_for(kind, N, Vb, H), mx_k, mw_k, g1, da, p->has_bias != 0, derr,
@@ -756,7 +809,7 @@ static flce_status_t backward_impl(const char* name, const flce_params_t* p, con
       db_parts = g1.tiles_m * 4;
     }
     if (p->has_bias &&
-        (launch_db_finalize(w.db_part, db_parts, static_cast<int>(bv), v0, Vb, db,
+        (launch_db_finalize(w.db_part, db_parts, ld_db, v0, Vb, db,
                             p->db_fp32 != 0, f16, s) != cudaSuccess ||
          !tr.after(FLCE_KERNEL_BWD_DB)))
       return FLCE_ERR_CUDA;

@@ -65,10 +65,12 @@ def _shard_params(N, H, V_local, vocab_start, vocab_total, has_bias, fp16, opts,
 
 
 def kept_size(N, H, V_local, *, vocab_start, vocab_total, bwd_vocab_block=0,
-              input_fp16=False) -> int:
-    """Bytes of a shard's kept state (flce_kept_size for the shard's rows)."""
+              input_fp16=False, keep_vocab=0) -> int:
+    """Bytes of a shard's kept state (flce_kept_size for the shard's rows;
+    ``keep_vocab`` widens the kept block as in flce_forward, give it to
+    forward_shard and backward_shard too)."""
     p = params(N, H, V_local, vocab_start=vocab_start, vocab_total=vocab_total,
-               bwd_vocab_block=bwd_vocab_block, input_fp16=input_fp16)
+               bwd_vocab_block=bwd_vocab_block, input_fp16=input_fp16, keep_vocab=keep_vocab)
     return int(_lib.load().flce_kept_size(p))
 
 

@@ -13,7 +13,7 @@ import torch
 from linear_cross_entropy_gemm_gb300 import inputs as I
 
 # Backward modes of the library (DeviceProblem.run).
-MODE_NAMES = ("recompute", "stored", "kept")
+MODE_NAMES = ("recompute", "stored", "kept", "budget")
 
 LOSS_RTOL = 1e-3
 GRAD_FROB = 5e-3
@@ -43,32 +43,38 @@ class DeviceProblem:
         self.dloss = torch.from_numpy(inp.dloss).to(self.dev)
 
     def run(self, *, dW_dtype=torch.float32, db_dtype=torch.float32, bwd_vocab_block=0,
-            mode="recompute", **over):
+            mode="recompute", keep_vocab=0, **over):
         """Forward + backward through the C ABI in one of the backward modes:
         "recompute" (every vocabulary block's logits recomputed), "stored"
-        (every logit's probability kept by the forward, no recompute) or
-        "kept" (the first vocabulary block's probabilities kept, the others
-        recomputed)."""
+        (every logit's probability kept by the forward, no recompute), "kept"
+        (the probabilities of the kept block [0, keep_vocab) kept, by default
+        one backward block, the other blocks recomputed) or "budget" (kept,
+        as wide as flce_keep_vocab_within allows with its default extra)."""
         import linear_cross_entropy_gemm_gb300 as F
         assert mode in MODE_NAMES, mode
         opts = opts_of(self.inp.wl)
         opts.update(over)
         wl = self.inp.wl
         saved = kept = None
+        if mode == "budget" and wl.N > 0:
+            keep_vocab = F.flce_keep_vocab_within(wl.N, wl.H, wl.V, has_bias=wl.has_bias,
+                                                  bwd_vocab_block=bwd_vocab_block,
+                                                  input_fp16=wl.dtype == "fp16")
         if mode == "stored":
             n = F.flce_saved_size(wl.N, wl.H, wl.V, label_smoothing=opts["label_smoothing"],
                                   input_fp16=wl.dtype == "fp16")
             saved = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
-        elif mode == "kept" and wl.N > 0:
+        elif mode in ("kept", "budget") and wl.N > 0:
             n = F.flce_kept_size(wl.N, wl.H, wl.V, input_fp16=wl.dtype == "fp16",
-                                 bwd_vocab_block=bwd_vocab_block)
+                                 bwd_vocab_block=bwd_vocab_block, keep_vocab=keep_vocab)
             kept = torch.empty(max(n, 1), dtype=torch.uint8, device=self.dev)
+        kv = keep_vocab if kept is not None else 0
         loss, lse = F.flce_forward(self.x, self.W, self.b, self.y, saved=saved, kept=kept,
-                                   bwd_vocab_block=bwd_vocab_block, **opts)
+                                   bwd_vocab_block=bwd_vocab_block, keep_vocab=kv, **opts)
         dx, dW, db = F.flce_backward(self.dloss, lse, self.x, self.W, self.b, self.y,
                                      dW_dtype=dW_dtype, db_dtype=db_dtype,
                                      bwd_vocab_block=bwd_vocab_block, saved=saved, kept=kept,
-                                     **opts)
+                                     keep_vocab=kv, **opts)
         torch.cuda.synchronize(self.dev)
         err = F.flce_read_device_error(self.dev)
         return dict(loss=loss, lse=lse, dx=dx, dW=dW, db=db, err=err)

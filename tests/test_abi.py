@@ -58,11 +58,28 @@ def test_binding_codes_match_the_header_enums():
     assert {k.lower(): v for k, v in red.items()} == _lib.REDUCTION
 
 
-def test_params_struct_layout_matches_header():
-    assert ctypes.sizeof(_lib.FlceParams) == 96
-    assert _lib.FlceParams.bwd_vocab_block.offset == 64
-    assert _lib.FlceParams.vocab_total.offset == 80
-    assert _lib.FlceParams.input_fp16.offset == 88
+def test_params_struct_layout_matches_header(tmp_path):
+    # The ctypes mirror against the C compiler's own layout of the header's
+    # struct: every field's offset and the total size.
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = [f for f, _ in _lib.FlceParams._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text("#include <stddef.h>\n#include <stdio.h>\n#include \"flce.h\"\n"
+                   "int main(void) {\n"
+                   + "".join(f'  printf("%zu\\n", offsetof(flce_params_t, {f}));\n'
+                             for f in fields)
+                   + '  printf("%zu\\n", sizeof(flce_params_t));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)], check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    want = [getattr(_lib.FlceParams, f).offset for f in fields] + [ctypes.sizeof(_lib.FlceParams)]
+    assert got == want, dict(zip(fields + ["sizeof"], zip(got, want)))
+    assert ctypes.sizeof(_lib.FlceParams) == 104
 
 
 def test_status_strings(lib):
@@ -88,6 +105,7 @@ def test_workspace_sizes(lib):
     (dict(N=-1), 1), (dict(H=0), 1), (dict(V=0), 1), (dict(H=12), 2),
     (dict(label_smoothing=1.5), 1), (dict(lse_square_scale=-1.0), 1),
     (dict(bwd_vocab_block=100), 1), (dict(gemm_form=4), 1), (dict(gemm_form=-1), 1),
+    (dict(keep_vocab=100), 1), (dict(keep_vocab=-256), 1),
 ])
 def test_invalid_params_rejected_on_host(lib, kw, status):
     base = dict(N=4, H=64, V=10)
@@ -156,6 +174,62 @@ def test_kept_and_stored_sizes(lib):
     shard = _lib.params(4, 64, 10, vocab_start=10, vocab_total=40)
     assert lib.flce_kept_size(shard) == lib.flce_kept_size(_lib.params(4, 64, 10)) > 0
     assert lib.flce_saved_size(shard) == 0
+
+
+def test_wider_kept_block_sizes(lib):
+    # keep_vocab = K keeps [N, K] fp16 plus maxima per 32 columns; below BVc
+    # it keeps BVc, at or above the vocabulary it is the stored state.
+    N, H, V = 8192, 4096, 128256
+    bv = 65536
+    vr = (V + 255) // 256 * 256
+
+    def kept(k, **kw):
+        return lib.flce_kept_size(_lib.params(N, H, V, keep_vocab=k, **kw))
+
+    assert kept(0) == kept(256) == kept(bv)
+    k = 98304
+    assert N * k * 2 + N * (k // 32) * 4 <= kept(k) <= N * k * 2 + N * (k // 32) * 4 + 1024
+    assert kept(vr) == kept(1 << 20) == lib.flce_saved_size(_lib.params(N, H, V))
+    # the kept backward's workspace: a dx accumulator only while blocks remain
+    # to recompute; db column partials as wide as the kept block
+    ws = lambda k, **kw: lib.flce_workspace_size(_lib.params(N, H, V, keep_vocab=k, **kw), 2)
+    assert ws(vr) == lib.flce_workspace_size(_lib.params(N, H, V), 3)
+    assert ws(k) - ws(vr) >= N * H * 4
+    rows = 4 * (N // 128)
+    assert ws(k, has_bias=True) - ws(k) >= rows * k * 4
+    assert ws(k, has_bias=True) - ws(k) - rows * k * 4 < 2048
+
+
+def _kept_mode_bytes(lib, p):
+    return lib.flce_kept_size(p) + lib.flce_workspace_size(p, 2)
+
+
+@pytest.mark.parametrize("N,H,V,kw", [
+    (8192, 4096, 128256, {}), (32768, 2048, 128000, dict(has_bias=True)),
+    (16384, 4096, 262144, {}), (4096, 2048, 32000, dict(has_bias=True)),
+    (512, 256, 4096, dict(bwd_vocab_block=1024)), (300, 64, 1000, dict(bwd_vocab_block=256)),
+])
+def test_keep_vocab_within_budget(lib, N, H, V, kw):
+    # The rule: the widest of V, V - BVc, V - 2 BVc, ... (rounded up to 256,
+    # at least BVc) whose kept-mode memory stays within the recompute
+    # workspace plus the extra bytes; one block (BVc) when none fits.
+    from linear_cross_entropy_gemm_gb300 import tuning
+    p = _lib.params(N, H, V, **kw)
+    base = lib.flce_workspace_size(p, 1)
+    vr = (V + 255) // 256 * 256
+    bvc = min(kw.get("bwd_vocab_block") or tuning.library_default_block(N, V), vr)
+    cands = [min(vr, (V - j * bvc + 255) // 256 * 256) for j in range(V // bvc + 1)
+             if V - j * bvc > bvc] or [vr]
+    widths = []
+    for extra in sorted((0, 1 << 20, 1 << 28, 4 * V * H, 1 << 34, 1 << 40)):
+        k = lib.flce_keep_vocab_within(p, extra)
+        fit = [c for c in cands
+               if _kept_mode_bytes(lib, _lib.params(N, H, V, keep_vocab=c, **kw)) <= base + extra]
+        assert k == (max(fit) if fit else bvc), (extra, k, fit)
+        widths.append(k)
+    assert widths == sorted(widths)  # more memory never keeps less
+    assert widths[-1] == vr
+    assert lib.flce_keep_vocab_within(_lib.params(0, H, V), 1 << 40) == 0
 
 
 def test_kept_entry_points_reject_bad_arguments_on_host(lib):

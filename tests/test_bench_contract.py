@@ -77,3 +77,23 @@ def test_gpu_vocab_split_line_matches_the_replica_loss():
         assert split["config"]["parallelism"].startswith("vocabulary split")
         assert split["roofline"]["bound"] == "tensor" and split["gpu_launches"] > 0
         assert abs(split["loss"] - plain["loss"]) <= 1e-6 * abs(plain["loss"])
+
+
+@pytest.mark.gpu
+def test_gpu_budget_mode_line():
+    # The kept block as wide as the method's budget allows: at this shape and
+    # block, part of the vocabulary (the rest is recomputed in 8192-column
+    # blocks); the line reports the width and stays within its bound.
+    import linear_cross_entropy_gemm_gb300 as F
+    N, H, V, bv = 2048, 256, 65536, 8192
+    k = F.flce_keep_vocab_within(N, H, V, bwd_vocab_block=bv)
+    assert bv < k < V
+    d = _run(["--steps", "3", "--warmup", "3", "--shape", f"{N},{H},{V}", "--no-cpu-baseline",
+              "--mode", "budget", "--only-mode", "--bwd-vocab-block", str(bv)])
+    assert d["impl_config"]["mode"] == "budget" and d["impl_config"]["keep_vocab"] == k
+    nblk = 1 + -(-(V - k) // bv)
+    assert d["gpu_launches"] == 3 * (4 + 3 * nblk)  # fwd, merge, finalize, prep; 3 per block
+    m = d["memory"]
+    assert m["device_free_drop_during_step_mib"] == 0
+    assert m["scratch_mib"] <= m["scratch_bound_mib"]
+    assert d["flops_executed_per_step"] == 8.0 * N * H * V - 2.0 * N * H * k

@@ -20,13 +20,18 @@ pytestmark = pytest.mark.gpu
 
 
 MODES = ["recompute", "stored", "kept"]
+# The full-size checks also run the kept block as wide as the method's memory
+# budget allows (flce_keep_vocab_within): the whole vocabulary at the Llama-3
+# head, one block at large_logit, half the vocabulary at vocab256k.
+FULL_MODES = MODES + ["budget"]
 
 
 def full_check(wl, *, bwd_vocab_block=0, dW_dtype=torch.float32, db_dtype=torch.float32,
-               mode="recompute", gemm_form="default"):
+               mode="recompute", gemm_form="default", keep_vocab=0):
     inp = I.make_inputs(wl)
     out = DeviceProblem(inp).run(bwd_vocab_block=bwd_vocab_block, dW_dtype=dW_dtype,
-                                 db_dtype=db_dtype, mode=mode, gemm_form=gemm_form)
+                                 db_dtype=db_dtype, mode=mode, gemm_form=gemm_form,
+                                 keep_vocab=keep_vocab)
     assert out["err"] == 0, f"device error word {out['err']}"
     x64, W64, b64 = f64(inp)
     opts = opts_of(wl)
@@ -127,6 +132,47 @@ def test_fp16_small_gradients_do_not_flush(mode):
     full_check(wl, mode=mode)
 
 
+@pytest.mark.parametrize("keep_vocab", [512, 768, 1280, 1536])
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_wider_kept_block_ragged(keep_vocab, reduction):
+    # A kept block wider than one backward block: the forward keeps [0, K),
+    # the backward converts it in place and recomputes [K, V) in 256-column
+    # blocks staged at the start of the kept buffer. V = 1300: K = 512 leaves
+    # 788 columns (256 + 256 + 256 + 20), K = 768 leaves 532, K = 1280 leaves
+    # 20, K = 1536 keeps everything. Bias, smoothing and z-loss exercise the
+    # kept-width db partials.
+    wl = I.Workload("wide_kept", N=129, H=72, V=1300, seed=41, b_std=0.5, ignore_frac=0.1,
+                    label_smoothing=0.2, lse_square_scale=1e-2, logit_scale=1.3,
+                    reduction=reduction,
+                    dloss="normal_per_token" if reduction == "none" else "normal_scalar")
+    full_check(wl, bwd_vocab_block=256, mode="kept", keep_vocab=keep_vocab)
+
+
+@pytest.mark.parametrize("gemm_form", ["default", "single", "pair", "wide"])
+def test_wider_kept_block_many_tiles(gemm_form):
+    # Several tiles in every direction: medium's options (bias, smoothing,
+    # z-loss) at 1000 x 2048 x 32000 with 4096-column blocks and a 12288-wide
+    # kept block (then 4 x 4096 recomputed and a 3328-column ragged block).
+    wl = I.WORKLOADS["medium"].with_(N=1000)
+    full_check(wl, bwd_vocab_block=4096, mode="kept", keep_vocab=12288, gemm_form=gemm_form)
+
+
+def test_wider_kept_block_fp16():
+    wl = I.WORKLOADS["medium"].with_(name="medium_fp16", dtype="fp16", N=1000, V=5000)
+    full_check(wl, bwd_vocab_block=1024, mode="kept", keep_vocab=2560,
+               dW_dtype=torch.float16, db_dtype=torch.float16)
+
+
+def test_budget_mode_keeps_the_rule_width():
+    # "budget": the width flce_keep_vocab_within picks. At this shape (bias,
+    # 1024-column blocks) the method's fp32 dW allowance (4 V H bytes) buys
+    # part of the vocabulary but not all of it.
+    wl = I.WORKLOADS["medium"].with_(N=2000, H=256, V=6000)
+    k = F.flce_keep_vocab_within(wl.N, wl.H, wl.V, has_bias=True, bwd_vocab_block=1024)
+    assert 1024 < k < 6000
+    full_check(wl, bwd_vocab_block=1024, mode="budget")
+
+
 def test_fp16_product_beyond_fp16_range_before_bias():
     # x W^T ~ 7e4 (> 65504) with a cancelling bias: fp32 accumulation keeps the
     # logits finite (DeepSpeed PR #8792's fp32-output GEMM lesson).
@@ -195,7 +241,7 @@ def test_run_to_run_bitwise_determinism(mode):
         assert torch.equal(a[k], b[k]), f"{k} differs between runs"
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", MODES + ["budget"])
 def test_autograd_module_matches_c_abi(mode):
     wl = I.Workload("module", N=256, H=128, V=1000, seed=27, b_std=0.05, ignore_frac=0.05,
                     label_smoothing=0.1, lse_square_scale=1e-3, logit_scale=0.9)
@@ -207,7 +253,8 @@ def test_autograd_module_matches_c_abi(mode):
     b = p.b.clone().requires_grad_(True)
     mod = F.FusedLinearCrossEntropyLoss(label_smoothing=0.1, lse_square_scale=1e-3,
                                         logit_scale=0.9, recompute=mode != "stored",
-                                        keep_block=mode == "kept")
+                                        keep_block=mode in ("kept", "budget"),
+                                        keep_vocab="budget" if mode == "budget" else 0)
     loss = mod(x.view(2, 128, 128), p.y.view(2, 128), W, b)
     loss.backward()
     torch.cuda.synchronize()
@@ -222,7 +269,7 @@ def test_autograd_module_matches_c_abi(mode):
 _cache = {}
 
 
-def _sampled(name, wl=None, modes=MODES):
+def _sampled(name, wl=None, modes=FULL_MODES):
     """GPU outputs plus the oracle on every token's statistics, 256 sampled
     dx rows and 256 sampled dW / db rows, for one full-size problem (a named
     workload, or `wl` under that name) in the given backward modes."""
@@ -270,7 +317,7 @@ def _sampled(name, wl=None, modes=MODES):
     return res
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode", FULL_MODES)
 @pytest.mark.parametrize("name", ["llama3_head", "large_logit", "vocab256k"])
 def test_full_size_sampled(name, mode):
     r = _sampled(name)
@@ -322,9 +369,10 @@ def test_non_contiguous_inputs_are_rejected():
         F.flce_forward(x, W, None, y)
 
 
-@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("mode,keep_vocab", [("recompute", 0), ("stored", 0), ("kept", 0),
+                                             ("kept", 768)])
 @pytest.mark.parametrize("N", [300, 129, 1])
-def test_no_writes_outside_caller_buffers(N, mode):
+def test_no_writes_outside_caller_buffers(N, mode, keep_vocab):
     # Every buffer the library writes gets a canary-filled guard region after
     # it (N = 300: an odd number of 128-row tiles, so a CTA pair's second half
     # is pure padding); the guards must be untouched after forward + backward.
@@ -346,7 +394,11 @@ def test_no_writes_outside_caller_buffers(N, mode):
 
     nf = F.flce_workspace_size(N, wl.H, wl.V, "forward", **opts)
     kind = {"kept": "backward_keep", "stored": "backward_store"}.get(mode, "backward")
-    nb = F.flce_workspace_size(N, wl.H, wl.V, kind, bwd_vocab_block=512, **opts)
+    nb = F.flce_workspace_size(N, wl.H, wl.V, kind, bwd_vocab_block=512, keep_vocab=keep_vocab,
+                               has_bias=wl.has_bias, **opts)
+    # (the binding would allocate a workspace of its own if this one were
+    # smaller than the call needs, and the guard would then check nothing)
+    assert wl.has_bias
     wf, wb = guarded(nf), guarded(nb)
     state, ns, skw = None, 0, {}
     if mode == "stored":
@@ -354,9 +406,9 @@ def test_no_writes_outside_caller_buffers(N, mode):
         state = guarded(ns)
         skw = dict(saved=state[:ns])
     elif mode == "kept":
-        ns = F.flce_kept_size(N, wl.H, wl.V, bwd_vocab_block=512, **opts)
+        ns = F.flce_kept_size(N, wl.H, wl.V, bwd_vocab_block=512, keep_vocab=keep_vocab, **opts)
         state = guarded(ns)
-        skw = dict(kept=state[:ns])
+        skw = dict(kept=state[:ns], keep_vocab=keep_vocab)
     lossb, lseb = guarded(4), guarded(4 * N)
     dxb, dWb, dbb = guarded(2 * N * wl.H), guarded(4 * wl.V * wl.H), guarded(4 * wl.V)
     loss = lossb[:4].view(torch.float32)
@@ -376,5 +428,5 @@ def test_no_writes_outside_caller_buffers(N, mode):
         check(t, n, what)
     if state is not None:
         check(state, ns, f"{mode} state")
-    ref = p.run(bwd_vocab_block=512, mode=mode)
+    ref = p.run(bwd_vocab_block=512, mode=mode, keep_vocab=keep_vocab)
     assert torch.equal(ref["dW"], dW) and torch.equal(ref["db"], db)

@@ -26,7 +26,7 @@ def _sim_allreduce(tensors):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("mode", ["recompute", "kept"])
+@pytest.mark.parametrize("mode", ["recompute", "kept", "wider kept"])
 @pytest.mark.parametrize("form", ["default", "single", "wide"])
 @pytest.mark.parametrize("reduction", ["mean", "sum", "none"])
 def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, dtype, monkeypatch):
@@ -48,17 +48,20 @@ def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, dtype, monk
     cuts = [0, 1000, 2256, 3001]
     shards = [(a, b - a) for a, b in zip(cuts[:-1], cuts[1:])]
 
-    # Kept mode: each shard keeps its own first 512-column block (the second
-    # and third shards are wider than one block, the first is exactly 1000).
+    # Kept mode: each shard keeps its own first 512-column block (the shards
+    # are 1000, 1256 and 745 columns wide); "wider kept": its first 768
+    # columns (all of the third shard).
     bvb = 512
-    kept = [VP.kept_size(wl.N, wl.H, n, vocab_start=a, vocab_total=wl.V, bwd_vocab_block=bvb)
-            for a, n in shards] if mode == "kept" else [0] * len(shards)
+    kv = {"kept": 0, "wider kept": 768}.get(mode)
+    sopts = dict(opts, keep_vocab=kv or 0)  # the shard calls' options
+    kept = [VP.kept_size(wl.N, wl.H, n, vocab_start=a, vocab_total=wl.V, bwd_vocab_block=bvb,
+                         keep_vocab=kv) for a, n in shards] if kv is not None else [0] * len(shards)
     kept = [torch.empty(k, dtype=torch.uint8, device=prob.dev) if k else None for k in kept]
 
     # forward: local stats, MAX of m, rescale, SUM of (d, z_y, sum z)
     stats = [VP.forward_shard(prob.x, prob.W[a:a + n].contiguous(), prob.b[a:a + n].contiguous(),
                               prob.y, vocab_start=a, vocab_total=wl.V, kept=k,
-                              bwd_vocab_block=bvb, **opts)
+                              bwd_vocab_block=bvb, **sopts)
              for (a, n), k in zip(shards, kept)]
     gmax = [s[0].clone() for s in stats]
     _sim_allreduce(gmax)("max")
@@ -70,7 +73,7 @@ def test_uneven_shards_match_whole_vocabulary(reduction, form, mode, dtype, monk
     # backward: per-shard dW rows, db, fp32 dx partials summed then cast once
     parts = [VP.backward_shard(prob.dloss, lse, prob.x, prob.W[a:a + n].contiguous(),
                                prob.b[a:a + n].contiguous(), prob.y, vocab_start=a,
-                               vocab_total=wl.V, kept=k, bwd_vocab_block=bvb, **opts)
+                               vocab_total=wl.V, kept=k, bwd_vocab_block=bvb, **sopts)
              for (a, n), k in zip(shards, kept)]
     dx32 = [p[0] for p in parts]
     _sim_allreduce(dx32)("sum")
