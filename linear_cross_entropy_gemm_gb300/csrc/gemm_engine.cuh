@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       Epi::tile(ea, g, tm, tn, row_in_tile, lane, quad, taddr, stage + (warp - 2) * kStageBytes,
                 sl);
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      tmem_release_arrive(&tempty[acc]);
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
@@ -496,7 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       Epi::tile(ea, g, tm2 * 2 + static_cast<int>(rank), tn, row_in_tile, lane, quad, taddr,
                 stage + (warp - 2) * kStageBytes, sl);
       tc_fence_before();
-      mbar_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
+      tmem_release_arrive_cluster(tempty0 + static_cast<uint32_t>(acc) * 8u);
       acc ^= 1;
       if (acc == 0) aph ^= 1;
     }
@@ -761,7 +761,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(wide_threads(kEW), 1
         ++sl.xcount;
       }
       tc_fence_before();
-      mbar_arrive_cluster(tempty0);
+      tmem_release_arrive_cluster(tempty0);
       aph ^= 1;
     }
     if (lane == 0) bulk_wait_group0();  // this warp's epilogue stores have completed
