@@ -296,7 +296,7 @@ class Problem:
     `shard` = (start, end) only W's rows [start, end) are on the device and a
     step runs the vocabulary-shard calls (vocab_parallel)."""
 
-    def __init__(self, torch, F, wl, dev, tdt, fkw, bkw, shard=None):
+    def __init__(self, torch, F, wl, dev, tdt, fkw, bkw, shard=None, dw_dtype=None):
         from linear_cross_entropy_gemm_gb300 import inputs as I
         self.torch, self.F, self.wl, self.dev = torch, F, wl, dev
         self.fkw, self.bkw = fkw, bkw
@@ -314,6 +314,8 @@ class Problem:
         self.dloss = self.host_dl.to(dev)
         self.opts = options_of(wl)
         self.tdt = tdt
+        # dW (and db) output type: fp32, or the operands' 16-bit type.
+        self.dw_dtype = torch.float32 if dw_dtype is None else dw_dtype
         self.bufs = None
 
     def keep_vocab(self, mode):
@@ -369,8 +371,8 @@ class Problem:
         b["loss"] = torch.empty(N if wl.reduction == "none" else 1, dtype=torch.float32, device=dev)
         b["lse"] = torch.empty(N, dtype=torch.float32, device=dev)
         b["dx"] = torch.empty(N, H, dtype=self.tdt, device=dev)
-        b["dW"] = torch.empty(V, H, dtype=torch.float32, device=dev)
-        b["db"] = torch.empty(V, dtype=torch.float32, device=dev) if wl.has_bias else None
+        b["dW"] = torch.empty(V, H, dtype=self.dw_dtype, device=dev)
+        b["db"] = torch.empty(V, dtype=self.dw_dtype, device=dev) if wl.has_bias else None
         self.bufs = b
         return b
 
@@ -400,7 +402,8 @@ class Problem:
             b["loss"], b["lse"] = VP.vocab_parallel_forward(xb, self.W, self.b, yb, **sh,
                                                             **self.opts)
             b["dx"], b["dW"], b["db"] = VP.vocab_parallel_backward(
-                dlb, b["lse"], xb, self.W, self.b, yb, **sh, **self.opts)
+                dlb, b["lse"], xb, self.W, self.b, yb, dW_dtype=self.dw_dtype,
+                db_dtype=self.dw_dtype, **sh, **self.opts)
             return
         st = {} if b["state"] is None else {("saved" if b["mode"] == "stored" else "kept"):
                                             b["state"]}
@@ -410,8 +413,8 @@ class Problem:
                        trace=ftr, bwd_vocab_block=self.bkw.get("bwd_vocab_block", 0),
                        **st, **self.opts, **self.fkw)
         F.flce_backward(dlb, b["lse"], xb, self.W, self.b, yb, workspace=b["bws"],
-                        out=(b["dx"], b["dW"], b["db"]), trace=btr, **st, **self.opts,
-                        **self.bkw)
+                        out=(b["dx"], b["dW"], b["db"]), trace=btr, dW_dtype=self.dw_dtype,
+                        db_dtype=self.dw_dtype, **st, **self.opts, **self.bkw)
 
 
 def end_to_end(torch, stream, prob, steps, barrier):
@@ -527,7 +530,8 @@ def run_ours(args):
                              "V >= 256 per rank")
         args.only_mode = True
         shard = VP.shard_range(V, ws, rank)
-    prob = Problem(torch, F, wl, dev, tdt, fkw, bkw, shard=shard)
+    prob = Problem(torch, F, wl, dev, tdt, fkw, bkw, shard=shard,
+                   dw_dtype=tdt if args.dw_dtype == "16bit" else torch.float32)
     if args.autotune:
         res = tuning.autotune(prob.x, prob.W, prob.b, prob.y, dloss=prob.dloss, reps=3,
                               mode="kept" if args.mode == "kept" else "recompute", **prob.opts)
@@ -675,7 +679,8 @@ def run_ours(args):
                         if wl.dtype == "bf16" and (N, H, V) == (8192, 4096, 128256) else None),
         "dtype": wl.dtype, "data": "synthetic",
         "config": config_of(wl, ws, vocab_split),
-        "impl_config": {"mode": args.mode, "bwd_vocab_block": bv_used, "dW_dtype": "fp32",
+        "impl_config": {"mode": args.mode, "bwd_vocab_block": bv_used,
+                        "dW_dtype": "fp32" if args.dw_dtype == "fp32" else wl.dtype,
                         "keep_vocab": (prob.keep_vocab(args.mode) if shard is None else 0) or None,
                         "gemm_form": forms_used,
                         **({"vocab_shard": list(shard)} if vocab_split else {})},
@@ -731,6 +736,9 @@ def main():
     ap.add_argument("--autotune", action="store_true",
                     help="time the GEMM forms and backward vocabulary blocks first and run the "
                          "fastest (tuning.autotune); the table goes into the JSON line")
+    ap.add_argument("--dw-dtype", default="fp32", choices=["fp32", "16bit"],
+                    help="dW and db output type: fp32, or the operands' type (what the "
+                         "autograd module returns)")
     ap.add_argument("--bwd-vocab-block", type=int, default=0,
                     help="backward vocabulary block (multiple of 256); 0 = library default")
     args = ap.parse_args()
