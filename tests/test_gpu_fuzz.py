@@ -1,9 +1,11 @@
 """Seeded randomized parity sweep: small random shapes (N, H, V off the tile
 grid, including single rows / columns), random loss options, bias, operand
-type, backward mode (recompute, stored or kept block) and vocabulary block, each compared element by element
-with the CPU oracle. The GEMM form cycles through default / single / pair /
-wide by case index (the random draws do not depend on it). The case list is
-fixed by the seed, so failures reproduce."""
+type, backward mode (recompute, stored or kept block) and vocabulary block,
+each compared element by element with the CPU oracle. The GEMM form cycles
+through default / single / pair / wide by case index, and every other kept
+case keeps a wider block (512, 1024 or 1536 columns; the random draws do not
+depend on either). The case list is fixed by the seed, so failures
+reproduce."""
 import numpy as np
 import pytest
 import torch
@@ -44,12 +46,13 @@ def _cases(n=24, seed=20261202):
         # recompute and kept-block modes by index (no extra random draw).
         mode = "stored" if store else ("kept" if i % 2 else "recompute")
         form = ("default", "single", "pair", "wide")[i % 4]
-        out.append(pytest.param(wl, bvb, mode, form,
+        kv = 512 * (1 + (i // 4) % 3) if mode == "kept" and i % 4 == 3 else 0
+        out.append(pytest.param(wl, bvb, mode, form, kv,
                                 id=f"{wl.name}-N{wl.N}-H{wl.H}-V{wl.V}-{wl.dtype}"
-                                f"-{red}-bv{bvb}-{mode}-{form}"))
+                                f"-{red}-bv{bvb}-{mode}{kv or ''}-{form}"))
     return out
 
 
-@pytest.mark.parametrize("wl,bvb,mode,form", _cases())
-def test_random_shapes_and_options(wl, bvb, mode, form):
-    full_check(wl, bwd_vocab_block=bvb, mode=mode, gemm_form=form)
+@pytest.mark.parametrize("wl,bvb,mode,form,keep_vocab", _cases())
+def test_random_shapes_and_options(wl, bvb, mode, form, keep_vocab):
+    full_check(wl, bwd_vocab_block=bvb, mode=mode, gemm_form=form, keep_vocab=keep_vocab)

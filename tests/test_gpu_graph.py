@@ -21,7 +21,7 @@ def _problem(seed):
     return wl, inp
 
 
-@pytest.mark.parametrize("mode", ["recompute", "kept", "stored"])
+@pytest.mark.parametrize("mode", ["recompute", "kept", "wider kept", "stored"])
 @pytest.mark.parametrize("form", ["single", "pair", "wide"])
 def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form, mode):
     wl, inp = _problem(41)
@@ -35,13 +35,18 @@ def test_forward_backward_replay_in_a_cuda_graph_equals_eager(form, mode):
     N, H, V = wl.N, wl.H, wl.V
     fws = torch.empty(F.flce_workspace_size(N, H, V, "forward", has_bias=True, **opts),
                       dtype=torch.uint8, device=dev)
-    kind = {"kept": "backward_keep", "stored": "backward_store"}.get(mode, "backward")
+    # "wider kept": the kept block is [0, 1792), then 1024 + 184 columns
+    # are recomputed.
+    kv = 1792 if mode == "wider kept" else 0
+    kind = {"kept": "backward_keep", "wider kept": "backward_keep",
+            "stored": "backward_store"}.get(mode, "backward")
     bws = torch.empty(F.flce_workspace_size(N, H, V, kind, has_bias=True, bwd_vocab_block=1024,
-                                            **opts), dtype=torch.uint8, device=dev)
+                                            keep_vocab=kv, **opts), dtype=torch.uint8, device=dev)
     state = {}
-    if mode == "kept":
-        state = dict(kept=torch.empty(F.flce_kept_size(N, H, V, bwd_vocab_block=1024),
-                                      dtype=torch.uint8, device=dev))
+    if mode in ("kept", "wider kept"):
+        state = dict(kept=torch.empty(F.flce_kept_size(N, H, V, bwd_vocab_block=1024,
+                                                       keep_vocab=kv),
+                                      dtype=torch.uint8, device=dev), keep_vocab=kv)
     elif mode == "stored":
         state = dict(saved=torch.empty(F.flce_saved_size(N, H, V), dtype=torch.uint8,
                                        device=dev))

@@ -61,3 +61,44 @@ def test_peak_memory_within_the_block_budget(name, mode):
         ws_plain = F.flce_workspace_size(N, H, V, "backward", has_bias=wl.has_bias,
                                          label_smoothing=wl.label_smoothing)
         assert kept + ws <= ws_plain + N * (bv // 32) * 4 + (1 << 10)
+
+
+@pytest.mark.parametrize("name", ["medium", "llama3_head"])
+def test_autograd_module_peak_memory(name):
+    # The user-facing module (default: one kept block): forward + backward
+    # peaks at the library's scratch plus the gradients in the parameters'
+    # own type (dW and db written as bf16 by the library; no fp32 [V, H]
+    # temporary).
+    wl = I.WORKLOADS[name]
+    N, H, V = wl.N, wl.H, wl.V
+    dev = torch.device("cuda", 0)
+    p = DeviceProblem(I.make_inputs(wl))
+    x = p.x.clone().requires_grad_(True)
+    W = p.W.clone().requires_grad_(True)
+    b = None if p.b is None else p.b.clone().requires_grad_(True)
+    mod = F.FusedLinearCrossEntropyLoss(label_smoothing=wl.label_smoothing,
+                                        lse_square_scale=wl.lse_square_scale,
+                                        logit_scale=wl.logit_scale, reduction="mean")
+
+    def step():
+        loss = mod(x, p.y, W, b)
+        loss.backward()
+        return loss
+
+    step()  # first launches (module loading) outside the measurement
+    x.grad = W.grad = None
+    if b is not None:
+        b.grad = None
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    step()
+    torch.cuda.synchronize(dev)
+    assert F.flce_read_device_error(dev) == 0
+    assert W.grad.dtype == W.dtype and x.grad.dtype == x.dtype
+    peak = torch.cuda.max_memory_allocated(dev) - base
+    grads = (N * H + V * H + (V if b is not None else 0)) * 2
+    bv = tuning.library_default_block(N, V)
+    bound = scratch_bound(N, H, V, bv, wl.has_bias) + grads + (1 << 20)
+    assert peak <= bound, (peak / 2**20, bound / 2**20)
