@@ -534,7 +534,8 @@ def run_ours(args):
                    dw_dtype=tdt if args.dw_dtype == "16bit" else torch.float32)
     if args.autotune:
         res = tuning.autotune(prob.x, prob.W, prob.b, prob.y, dloss=prob.dloss, reps=3,
-                              mode="kept" if args.mode == "kept" else "recompute", **prob.opts)
+                              mode="kept" if args.mode in ("kept", "budget") else "recompute",
+                              **prob.opts)
         fkw.update(res.config.forward_kwargs())
         bkw.update(res.config.backward_kwargs())
         tune = res.as_dict()
