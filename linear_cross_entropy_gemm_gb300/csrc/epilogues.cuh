@@ -87,38 +87,44 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32], int lane) {
   return v[0];
 }
 
-// Reductions of 32 values as pairwise trees (depth 5 instead of a 31-long
-// dependent chain: with two epilogue warps per SM sub-partition the chain's
-// latency is not hidden).
+// Reductions of 32 values as trees (depth 4-5 instead of a 31-long dependent
+// chain: with two epilogue warps per SM sub-partition the chain's latency is
+// not hidden). The maximum and minimum take three inputs per instruction (16
+// instructions; exact in any order). The sum adds packed pairs in the same
+// association as the scalar tree t[i] = v[i] + v[i + 16], t[i] += t[i + w]
+// for w = 8, 4, 2, 1 (16 instructions instead of 31, the same bits).
 __device__ __forceinline__ float tree_max32(const float (&v)[32]) {
-  float t[16];
+  float t[12];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = fmaxf(v[i], v[i + 16]);
+  for (int k = 0; k < 10; ++k) t[k] = fmax3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  t[10] = v[30];
+  t[11] = v[31];
 #pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
-  return t[0];
+  for (int k = 0; k < 4; ++k) t[k] = fmax3(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
+  return fmaxf(fmax3(t[0], t[1], t[2]), t[3]);
 }
 __device__ __forceinline__ float tree_min32(const float (&v)[32]) {
-  float t[16];
+  float t[12];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = fminf(v[i], v[i + 16]);
+  for (int k = 0; k < 10; ++k) t[k] = fmin3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+  t[10] = v[30];
+  t[11] = v[31];
 #pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
-#pragma unroll
-    for (int i = 0; i < w; ++i) t[i] = fminf(t[i], t[i + w]);
-  return t[0];
+  for (int k = 0; k < 4; ++k) t[k] = fmin3(t[3 * k], t[3 * k + 1], t[3 * k + 2]);
+  return fminf(fmin3(t[0], t[1], t[2]), t[3]);
 }
 __device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
-  float t[16];
+  uint64_t t[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) t[i] = v[i] + v[i + 16];
+  for (int i = 0; i < 8; ++i)
+    t[i] = fadd2(f32x2(v[2 * i], v[2 * i + 1]), f32x2(v[2 * i + 16], v[2 * i + 17]));
 #pragma unroll
-  for (int w = 8; w > 0; w >>= 1)
+  for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
-    for (int i = 0; i < w; ++i) t[i] += t[i + w];
-  return t[0];
+    for (int i = 0; i < w; ++i) t[i] = fadd2(t[i], t[i + w]);
+  float lo, hi;
+  f32x2_split(t[0], lo, hi);
+  return lo + hi;
 }
 
 // p ? a : b as one selp. A chain of selects that picks v[j] for j == k would
@@ -275,8 +281,15 @@ struct FwdLseEpi {
       if (nm != -INFINITY) {
         float acc = d * fast_exp2(m - nm);
         if (full) {
+          // z log2e - nm for two logits per packed FFMA.
+          const uint64_t c2x2 = f32x2(c2, c2), nmx2 = f32x2(-nm, -nm);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = fast_exp2(fmaf(v[j], c2, -nm));
+          for (int j = 0; j < 16; ++j) {
+            float lo, hi;
+            f32x2_split(ffma2(f32x2(v[2 * j], v[2 * j + 1]), c2x2, nmx2), lo, hi);
+            v[2 * j] = fast_exp2(lo);
+            v[2 * j + 1] = fast_exp2(hi);
+          }
           acc += tree_sum32(v);
         } else {
 #pragma unroll
@@ -391,8 +404,18 @@ struct DlogitsEpi {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] += bv[j];
       }
+      {
+        // a 2^(c2 u - lse2) - c for two logits per packed FFMA pair.
+        const uint64_t c2x2 = f32x2(c2, c2), lx2 = f32x2(-cf.x, -cf.x);
+        const uint64_t ax2 = f32x2(cf.y, cf.y), cx2 = f32x2(-cf.z, -cf.z);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = fmaf(cf.y, fast_exp2(fmaf(v[j], c2, -cf.x)), -cf.z);
+        for (int j = 0; j < 16; ++j) {
+          float lo, hi;
+          f32x2_split(ffma2(f32x2(v[2 * j], v[2 * j + 1]), c2x2, lx2), lo, hi);
+          f32x2_split(ffma2(f32x2(fast_exp2(lo), fast_exp2(hi)), ax2, cx2), v[2 * j],
+                      v[2 * j + 1]);
+        }
+      }
       if ((ty >> 5) == c) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] -= (j == (ty & 31)) ? cf.w : 0.f;
@@ -411,8 +434,10 @@ struct DlogitsEpi {
           tma_block_16(&a.dl_map, colb0, row0, v, a.fp16 != 0, stage, lane);
         } else {
           float sv[32];
+          const uint64_t dx2 = f32x2(dls, dls);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sv[j] = v[j] * dls;
+          for (int j = 0; j < 16; ++j)
+            f32x2_split(fmul2(f32x2(v[2 * j], v[2 * j + 1]), dx2), sv[2 * j], sv[2 * j + 1]);
           tma_block_16(&a.dl_map, colb0, row0, sv, a.fp16 != 0, stage, lane);
         }
       }
