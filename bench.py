@@ -89,8 +89,8 @@ MODES = ("kept", "recompute", "stored", "budget")
 # step in the kept-block mode (1-pass metrics, default GEMM forms and block,
 # the committed build of these kernels). Not measured by this run; reported
 # only for that exact configuration and labelled as such.
-TRAFFIC_CAPTURE = {"fwd_lse": 5.130e9, "bwd_dlogits": 3.068e9, "bwd_dw": 4.752e9,
-                   "bwd_dx": 5.985e9}
+TRAFFIC_CAPTURE = {"fwd_lse": 5.027e9, "bwd_dlogits": 2.977e9, "bwd_dw": 4.465e9,
+                   "bwd_dx": 6.483e9}
 TRAFFIC_SOURCE = ("ncu capture of the kept-block Llama-3 head step on a GB300 "
                   "(dram__bytes_read.sum + dram__bytes_write.sum per launch); not measured "
                   "in this run")
