@@ -365,14 +365,16 @@ class FusedLinearCrossEntropyFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, dloss):
         x, target, weight, bias, lse = ctx.saved_tensors
+        # dW and db are written in the parameters' own type by the library's
+        # epilogues (fp32 sums rounded once to nearest even, as a cast of the
+        # fp32 result would be), so no [V, H] fp32 temporary is allocated.
         dx, dW, db = flce_backward(dloss.float().contiguous(), lse, x, weight, bias, target,
-                                   dW_dtype=torch.float32, db_dtype=torch.float32,
+                                   dW_dtype=weight.dtype,
+                                   db_dtype=torch.float32 if bias is None else bias.dtype,
                                    saved=ctx.saved_state, kept=ctx.kept_state,
                                    keep_vocab=ctx.keep_vocab, **ctx.opts,
                                    **({} if ctx.config is None else ctx.config.backward_kwargs()))
         ctx.saved_state = ctx.kept_state = None
-        dW = dW.to(weight.dtype)
-        db = None if db is None else db.to(bias.dtype)
         return dx, None, dW, db, None, None, None, None, None, None, None, None, None
 
 

@@ -173,6 +173,31 @@ def test_budget_mode_keeps_the_rule_width():
     full_check(wl, bwd_vocab_block=1024, mode="budget")
 
 
+@pytest.mark.parametrize("mode", ["recompute", "kept"])
+@pytest.mark.parametrize("case", ["tiny", "ragged"])
+def test_against_the_cpp_reference(case, mode):
+    # The same element-by-element bounds against the second statement of the
+    # definition, the C++ fp64 reference (oracle/flce_oracle_ref.cpp).
+    from oracle import cpp as C
+    wl = I.WORKLOADS["tiny"] if case == "tiny" else I.Workload(
+        "ragged_cpp", N=129, H=72, V=1300, seed=43, b_std=0.5, ignore_frac=0.1,
+        label_smoothing=0.2, lse_square_scale=1e-2, logit_scale=1.3, reduction="none",
+        dloss="normal_per_token")
+    inp = I.make_inputs(wl)
+    out = DeviceProblem(inp).run(bwd_vocab_block=256 if case == "ragged" else 0, mode=mode)
+    assert out["err"] == 0
+    x64, W64, b64 = f64(inp)
+    opts = opts_of(wl)
+    rl, rlse = C.forward(x64, W64, b64, inp.y, **opts)
+    rdx, rdW, rdb = C.backward(inp.dloss.astype(np.float64), x64, W64, b64, inp.y, **opts)
+    assert_loss_close(to_np(out["loss"]), rl, f"{wl.name} loss (C++ reference)")
+    assert_loss_close(to_np(out["lse"]), rlse, f"{wl.name} lse (C++ reference)")
+    assert_grad_close(to_np(out["dx"]), rdx, f"{wl.name} dx (C++ reference)")
+    assert_grad_close(to_np(out["dW"]), rdW, f"{wl.name} dW (C++ reference)")
+    if wl.has_bias:
+        assert_grad_close(to_np(out["db"]), rdb, f"{wl.name} db (C++ reference)")
+
+
 def test_fp16_product_beyond_fp16_range_before_bias():
     # x W^T ~ 7e4 (> 65504) with a cancelling bias: fp32 accumulation keeps the
     # logits finite (DeepSpeed PR #8792's fp32-output GEMM lesson).
