@@ -4,8 +4,9 @@
 // Forward  (DeepSpeed PR #8792 "What": forward keeps per-token softmax
 //           statistics only):
 //   fwd_lse GEMM  x W^T tile by tile -> (m, d[, sum z]) partials + z_y; in the
-//                 kept-block mode also the first backward block's fp16
-//                 probabilities and their 32-column running maxima
+//                 kept-block mode also the kept block's fp16 probabilities
+//                 (the first backward block, or keep_vocab columns) and their
+//                 32-column running maxima
 //   merge         partials -> lse, per-token loss, reduction
 // Backward (same page: logits recomputed one vocabulary block at a time, so
 //           each dW block is one GEMM over all tokens):
@@ -18,7 +19,7 @@
 //     dx GEMM       dx (+)= dL_blk W_blk                  (fp32 across blocks)
 //     db finalize   (with a bias)
 // The stored-probability mode is the kept-block mode with one block over the
-// whole vocabulary.
+// whole vocabulary; keep_vocab sets any width in between.
 #include <algorithm>
 #include <cstdint>
 #include <cstdlib>
