@@ -5,7 +5,8 @@
  * lse = log V, the mean loss is log V, dx = 0 and, for reduction mean over T
  * non-ignored tokens, dW[v, :] = s * sum_n (1/V - [v == y_n]) x[n, :] / T
  * (gradient of cross-entropy at uniform logits; fla cross_entropy_kernel).
- * Run twice: the plain forward / backward and the kept-block pair. */
+ * Run three times: the plain forward / backward, the kept-block pair, and
+ * the kept-block pair with a kept block of 512 columns (keep_vocab). */
 #include <math.h>
 #include <stdint.h>
 #include <stdio.h>
@@ -23,7 +24,8 @@ static float bf2f(uint16_t b) { uint32_t u = (uint32_t)b << 16; float f; memcpy(
 #define FL(x) do { flce_status_t s_ = (x); if (s_ != FLCE_OK) { fprintf(stderr, "flce %s at %d\n", flce_status_string(s_), __LINE__); return 3; } } while (0)
 
 /* One forward + backward (plain, or the kept-block pair with 256-column
- * vocabulary blocks) checked against the closed form. */
+ * vocabulary blocks; keep = 2 keeps [0, 512) and recomputes the rest)
+ * checked against the closed form. */
 static int run(int keep) {
   const int64_t N = 200, H = 72, V = 1000;
   flce_params_t p;
@@ -31,6 +33,12 @@ static int run(int keep) {
   p.N = N; p.H = H; p.V = V; p.ignore_index = -100; p.logit_scale = 0.5f;
   p.reduction = FLCE_REDUCTION_MEAN; p.dW_fp32 = 1; p.db_fp32 = 1;
   if (keep) p.bwd_vocab_block = 256;
+  if (keep == 2) {
+    p.keep_vocab = 512;
+    /* the budget rule answers with a width the keep calls accept */
+    const int64_t kw = flce_keep_vocab_within(&p, (size_t)(4 * V * H));
+    if (kw < 256 || kw % 256 != 0) { fprintf(stderr, "keep_vocab_within %lld\n", (long long)kw); return 4; }
+  }
 
   uint16_t* hx = malloc(N * H * 2);
   int64_t* hy = malloc(N * 8);
@@ -93,8 +101,9 @@ static int run(int keep) {
     }
   if (sqrt(num / den) > 5e-3 || mx > mref / 128.0) { fprintf(stderr, "dW rel-Frobenius %g max %g\n", sqrt(num / den), mx); bad = 1; }
   if (herr != 0) { fprintf(stderr, "device error %d\n", herr); bad = 1; }
-  printf("%s (%s): loss %.6f (log V %.6f), %s\n", bad ? "FAIL" : "ok", keep ? "kept block" : "plain",
-         hloss, logV, flce_version());
+  printf("%s (%s): loss %.6f (log V %.6f), %s\n", bad ? "FAIL" : "ok",
+         keep == 2 ? "kept block of 512 columns" : keep ? "kept block" : "plain", hloss, logV,
+         flce_version());
   cudaFree(x); cudaFree(W); cudaFree(y); cudaFree(loss); cudaFree(lse); cudaFree(dloss);
   cudaFree(dx); cudaFree(dW); cudaFree(err); cudaFree(ws_f); cudaFree(ws_b);
   if (kept) cudaFree(kept);
@@ -105,5 +114,6 @@ static int run(int keep) {
 int main(void) {
   int bad = run(0);
   bad |= run(1);
+  bad |= run(2);
   return bad;
 }

@@ -28,4 +28,4 @@ def test_c_program_against_closed_form(tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     lines = r.stdout.splitlines()
-    assert len(lines) == 2 and all(l.startswith("ok") for l in lines), r.stdout
+    assert len(lines) == 3 and all(l.startswith("ok") for l in lines), r.stdout
