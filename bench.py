@@ -588,6 +588,23 @@ def run_ours(args):
                              e2e=e2e, loss=loss_value)
         prob.release()
 
+    if shard is None and prob.dw_dtype == torch.float32:
+        # The same step's peak with dW and db in the operands' 16-bit type
+        # (what the autograd module returns): one untimed step.
+        barrier()
+        torch.cuda.empty_cache()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        prob.dw_dtype = tdt
+        prob.allocate(args.mode)
+        prob.step()
+        barrier()
+        results[args.mode]["mem"]["peak_extra_mib_16bit_grads"] = (
+            torch.cuda.max_memory_allocated(dev) - base) / 2**20
+        results[args.mode]["mem"]["outputs_mib_16bit_grads"] = prob.output_bytes() / 2**20
+        prob.release()
+        prob.dw_dtype = torch.float32
+
     head = results[args.mode]
     ms, per_kernel = head["ms"], head["per_kernel"]
     steps_ = args.steps

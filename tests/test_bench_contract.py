@@ -62,6 +62,9 @@ def test_gpu_arm_line():
     # Peak = scratch + outputs, up to the caching allocator's granularity (a
     # large block keeps a remainder under 1 MiB unsplit).
     assert 0 <= m["peak_extra_mib"] - m["scratch_mib"] - m["outputs_mib"] < 8.0
+    # the same step with 16-bit dW and db: the same scratch, smaller outputs
+    assert m["outputs_mib_16bit_grads"] < m["outputs_mib"]
+    assert 0 <= m["peak_extra_mib_16bit_grads"] - m["scratch_mib"] - m["outputs_mib_16bit_grads"] < 8.0
 
 
 @pytest.mark.gpu
