@@ -256,3 +256,19 @@ def test_kept_entry_points_reject_bad_arguments_on_host(lib):
                                   None) == 3
     assert lib.flce_backward_store(p, f, f, f, ns - 1, f, f, None, f, f, f, None, f, ws, None,
                                    None, None) == 3
+
+
+def test_budget_widths_at_the_five_workloads(lib):
+    # The widths the budget rule (extra = 4 V H bytes) gives at the
+    # workloads, as measured and documented: the whole vocabulary at tiny,
+    # medium and the Llama-3 head, one 16384-column block at large_logit, half
+    # of vocab256k's vocabulary.
+    from linear_cross_entropy_gemm_gb300 import inputs as I
+    want = {"tiny": 4096, "medium": 32000, "llama3_head": 128256, "large_logit": 16384,
+            "vocab256k": 131072}
+    for name, k in want.items():
+        wl = I.WORKLOADS[name]
+        p = _lib.params(wl.N, wl.H, wl.V, has_bias=wl.has_bias)
+        got = lib.flce_keep_vocab_within(p, 4 * wl.V * wl.H)
+        vr = (wl.V + 255) // 256 * 256
+        assert min(got, vr) == min((k + 255) // 256 * 256, vr), (name, got)
